@@ -1,0 +1,387 @@
+#!/usr/bin/env python
+"""EntmaxKV decode-step benchmark.
+
+One step = score_pages -> select -> decode (the whole decode hot path) for the
+batched 128K-context workload: batch 8, 32 query / 8 kv heads, d = 128, 131072
+tokens per sequence, pages of 32, bf16 K/V, 8 planted high-score pages per
+(sequence, kv head), alpha = 1.5, 4096-token budget.  Inputs are seeded
+synthetic data resident in HBM; the 4 GiB K/V pool is far larger than L2 and
+L2 is also flushed (a 512 MiB write) between timed steps, outside the timed
+events.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle on a
+bounded sample of the same step instead.  With torchrun (N > 1) every rank runs
+an independent replica (the path needs no collective); the time is the max over
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse entmax decode µs/step and achieved HBM GB/s (frac of peak) at 128K ctx"
+FALLBACK_HBM_GBS = 6400.0
+KERNELS_PER_STEP = 6   # score, select, plan, qk, tau, pv
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="long128k")
+    ap.add_argument("--alpha", type=float, default=None)
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
+    ap.add_argument("--context", type=int, default=None, help="override the context length")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--flush-mb", type=int, default=512)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def overrides(args) -> dict:
+    kw = {}
+    if args.alpha is not None:
+        kw["alpha"] = args.alpha
+    if args.batch is not None:
+        kw["batch"] = args.batch
+    if args.context is not None:
+        kw["context"] = args.context
+    return kw
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: batch {w.batch}, {w.num_q_heads} q / {w.num_kv_heads} kv heads, "
+                        f"d={w.head_dim}, context {w.params['context']}, page {w.page_size}, "
+                        f"{w.dtype} K/V, alpha={w.alpha}, policy {w.policy}, "
+                        f"budget {w.budget_tokens} tokens",
+            "batch": w.batch, "context": w.params["context"], "page_size": w.page_size,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "alpha": w.alpha, "policy": w.policy,
+            "budget_tokens": w.budget_tokens, "kv_dtype": w.dtype, "seed": w.seed,
+            "l2": "inputs (4 GiB K/V) larger than L2, and L2 flushed between timed steps"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.proc = None
+        self.lines: list[str] = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if bus_id:
+            cmd += ["-i", bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def bus_id_of(dev: int) -> str | None:
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# oracle (CPU) timing: the cpu_baseline leg and the reference arm
+# ---------------------------------------------------------------------------
+def oracle_time_per_step(w, seconds: float, steps: int | None = None):
+    """Times the fp64 oracle's score -> select -> sparse attention on a bounded
+    sample of query heads; returns (us per full step, sample description, cores,
+    per-step list)."""
+    import numpy as np
+    import oracle
+    kv = oracle.KV(w)
+    meta = oracle.build_meta(kv)       # prefill work, not part of a decode step
+    BH = w.batch * w.num_q_heads
+    cores = oracle.get_threads()
+    t0 = time.perf_counter()
+    oracle.sparse_step(kv, w, heads=np.arange(min(BH, cores), dtype=np.int32), meta=meta)
+    per_head = max(1e-6, (time.perf_counter() - t0) / min(BH, cores))  # wall time per head, parallel
+    if steps is None:
+        n_heads = BH
+        reps = max(1, int(seconds / max(per_head * BH / max(1, cores), 1e-3)))
+        reps = min(reps, 50)
+    else:
+        budget = seconds / max(1, steps)
+        n_heads = int(min(BH, max(cores, budget / per_head * cores)))
+        reps = steps
+    rng = np.random.default_rng(0)
+    times = []
+    for _ in range(reps):
+        heads = np.sort(rng.choice(BH, size=n_heads, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.sparse_step(kv, w, heads=heads, meta=meta)
+        times.append((time.perf_counter() - t0) * 1e6 * BH / n_heads)
+    desc = (f"{n_heads} of {BH} query heads per step (score, top-k/tau-hat select, sparse "
+            f"attention; fp64), {reps} steps, scaled to a full step; metadata prebuilt")
+    return statistics.mean(times), desc, cores, times
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    from sparse_long_context_08_b300.workloads import make_workload
+    w = make_workload(args.workload, **overrides(args))
+    budget = 150.0
+    oracle_time_per_step(w, budget * 0.1, steps=max(1, args.warmup))   # warm-up steps
+    us, desc, cores, _ = oracle_time_per_step(w, budget, steps=args.steps)
+    line = {"metric": METRIC, "impl": "reference", "value": us, "unit": "us/step",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from sparse_long_context_08_b300 import entmaxkv as E
+    from sparse_long_context_08_b300.api import EntmaxKVDecoder, upload_workload
+    from sparse_long_context_08_b300.workloads import make_workload
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    E.lib()
+    from sparse_long_context_08_b300.workloads import CONFIGS
+    kw = overrides(args)
+    w = make_workload(args.workload, seed=CONFIGS[args.workload]["seed"] + 1000 * rank, **kw)
+    kv, q = upload_workload(w)
+    dec = EntmaxKVDecoder(kv, w.num_q_heads, float(w.scale), w.alpha, w.policy,
+                          w.budget_tokens, w.delta)
+    dec.build_meta()
+    torch.cuda.synchronize()
+    flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs is None:
+            dec.step(q)
+            return
+        evs[0].record()
+        dec.score(q)
+        evs[1].record()
+        dec.select()
+        E.entmaxkv_set_stage_events(evs[2:7])
+        dec.decode(q)
+        E.entmaxkv_set_stage_events(None)
+
+    for i in range(max(3, args.warmup)):
+        step()
+        flush.fill_(i & 255)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for e in ev:            # create the underlying events outside the timed region
+        for x in e:
+            x.record()
+    sampler = ClockSampler(bus_id_of(local_rank)) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    torch.cuda.synchronize()
+    for i in range(K):
+        step(ev[i])
+        flush.fill_((i + 7) & 255)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    # per-step stage times (ms): score | select | plan | qk | tau | pv
+    names = ["score", "select", "plan", "qk", "tau", "pv"]
+    stage = {n: [] for n in names}
+    total = []
+    for e in ev:
+        t = [e[j].elapsed_time(e[j + 1]) for j in range(6)]
+        for n, v in zip(names, t):
+            stage[n].append(v)
+        total.append(e[0].elapsed_time(e[6]))
+    t_sum = torch.tensor([sum(total)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t_sum, op=dist.ReduceOp.MAX)
+    ms_per_step = float(t_sum.item()) / K
+
+    # bytes the step reads (metadata + selected pages + small tensors)
+    up, vp = E.entmaxkv_decode_counts(dec.workspace, w.batch, w.num_q_heads, w.num_kv_heads,
+                                      w.head_dim, w.page_size, w.max_pages, dec.cap)
+    esz = 2 if w.dtype == "bf16" else 4
+    pages = sum(w.pages_of(b) for b in range(w.batch))
+    page_bytes = w.page_size * w.head_dim * esz
+    meta_row = 2 * w.head_dim * (esz if w.policy == "topk" else 4)
+    bytes_meta = pages * w.num_kv_heads * meta_row + pages * 4
+    bytes_k = int(up.sum()) * page_bytes
+    bytes_v = int(vp.sum()) * page_bytes
+    small = 2 * w.batch * w.num_q_heads * w.head_dim * 4
+    bytes_step = bytes_meta + bytes_k + bytes_v + small
+    mean = {n: statistics.mean(v) for n, v in stage.items()}
+    per_kernel_bytes = {"score": bytes_meta, "qk": bytes_k, "pv": bytes_v}
+    dom = max(mean, key=mean.get)
+    peak, peak_kind = measured_peak()
+    dom_bytes = per_kernel_bytes.get(dom)
+    achieved = dom_bytes / (mean[dom] * 1e-3) / 1e9 if dom_bytes else None
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as f:
+                tr = json.load(f)
+            if tr.get("workload") == args.workload and tr.get("kernel") == dom:
+                traffic = tr.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+                "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,
+                "algorithmic_bytes": dom_bytes}
+
+    # end to end through the public API: pinned host q in, pinned host out back
+    e2e = None
+    if not args.no_e2e:
+        q_host = q.cpu().pin_memory()
+        out_host = torch.empty(dec.out.shape, dtype=torch.float32).pin_memory()
+        q_dev = torch.empty_like(q)
+        for _ in range(3):
+            dec.step_host(q_host, out_host, q_dev)
+        torch.cuda.synchronize()
+        times = []
+        for i in range(K):
+            flush.fill_(i & 255)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            dec.step_host(q_host, out_host, q_dev)
+            stream.synchronize()
+            times.append(time.perf_counter() - t0)
+        t_e2e = torch.tensor([sum(times)], dtype=torch.float64, device="cuda")
+        if world > 1:
+            dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
+        e2e = {"value": float(t_e2e.item()) / K / world * 1e6, "unit": "us/step",
+               "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4,
+               "timing": "host wall clock per step incl. H2D, the three calls, D2H and sync"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us, desc, cores, _ = oracle_time_per_step(w, args.cpu_seconds)
+        cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    value_us = ms_per_step * 1e3 / world
+    line = {
+        "metric": METRIC, "value": value_us, "unit": "us/step", "n_gpus": world,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": workload_config(w),
+        "hbm_gbs": bytes_step / (ms_per_step * 1e-3) / 1e9,
+        "hbm_frac_of_measured": bytes_step / (ms_per_step * 1e-3) / 1e9 / peak,
+        "hbm_frac_of_8tbs": bytes_step / (ms_per_step * 1e-3) / 1e9 / 8000.0,
+        "bytes_per_step": bytes_step,
+        "bytes_breakdown": {"metadata_and_page_table": bytes_meta, "k_union_pages": bytes_k,
+                            "v_support_pages": bytes_v, "q_and_out": small,
+                            "union_pages": int(up.sum()), "v_pages": int(vp.sum())},
+        "stage_us": {n: v * 1e3 for n, v in mean.items()},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP * K, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

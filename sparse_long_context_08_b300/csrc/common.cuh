@@ -1,0 +1,257 @@
+// Shared device helpers for the EntmaxKV kernels (sm_103a): element widening,
+// warp/block reductions, order-preserving float keys, and the mbarrier + bulk
+// copy (TMA, cp.async.bulk) primitives used to stage K/V pages.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace ekv {
+
+// ---------------------------------------------------------------------------
+// elements: fp32, or bf16 stored as raw 16-bit patterns (widened exactly)
+// ---------------------------------------------------------------------------
+struct bf16raw { uint16_t bits; };
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kPer16 = 4;   // elements per 16-byte chunk
+    __device__ __forceinline__ static void widen(const uint4& r, float* o) {
+        o[0] = __uint_as_float(r.x); o[1] = __uint_as_float(r.y);
+        o[2] = __uint_as_float(r.z); o[3] = __uint_as_float(r.w);
+    }
+    __device__ __forceinline__ static float one(const float* p, int64_t i) { return p[i]; }
+    __device__ __forceinline__ static void store(float* p, int64_t i, float v) { p[i] = v; }
+};
+template <> struct Elem<bf16raw> {
+    static constexpr int kPer16 = 8;
+    __device__ __forceinline__ static void widen(const uint4& r, float* o) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o[2 * i] = __uint_as_float(w[i] << 16);
+            o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    __device__ __forceinline__ static float one(const bf16raw* p, int64_t i) {
+        return __uint_as_float(static_cast<uint32_t>(p[i].bits) << 16);
+    }
+    // only used for values that are themselves widened bf16 (exact)
+    __device__ __forceinline__ static void store(bf16raw* p, int64_t i, float v) {
+        p[i].bits = static_cast<uint16_t>(__float_as_uint(v) >> 16);
+    }
+};
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------
+template <int kLanes>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ uint32_t warp_max_u(uint32_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Block-wide reductions; `red` is shared scratch of >= 32 entries.  Every
+// thread of the block must call them; all threads receive the result.
+__device__ __forceinline__ float block_max(float v, float* red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v = warp_max(v);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    v = lane < nw ? red[lane] : -INFINITY;
+    return warp_max(v);
+}
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    v = lane < nw ? red[lane] : 0.f;
+    return warp_sum(v);
+}
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v.x = warp_sum(v.x);
+    v.y = warp_sum(v.y);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    v = lane < nw ? red[lane] : make_float2(0.f, 0.f);
+    v.x = warp_sum(v.x);
+    v.y = warp_sum(v.y);
+    return v;
+}
+__device__ __forceinline__ int block_sum_i(int v, int* red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v = warp_sum_i(v);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    v = lane < nw ? red[lane] : 0;
+    return warp_sum_i(v);
+}
+__device__ __forceinline__ uint32_t block_max_u(uint32_t v, uint32_t* red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v = warp_max_u(v);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    v = lane < nw ? red[lane] : 0u;
+    return warp_max_u(v);
+}
+
+// Exclusive block scan of one int per thread; returns the prefix and writes
+// the block total to *total.  `red` needs >= 33 ints.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* red, int* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    __syncthreads();
+    if (lane == 31) red[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int s = lane < nw ? red[lane] : 0;
+        int si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xFFFFFFFFu, si, o);
+            if (lane >= o) si += n;
+        }
+        if (lane < nw) red[lane] = si - s;
+        if (lane == 31) red[32] = si;
+    }
+    __syncthreads();
+    int r = red[wid] + incl - v;
+    *total = red[32];
+    return r;
+}
+
+// Same for floats (inclusive prefix of one value per thread).
+__device__ __forceinline__ float block_inclusive_scan_f(float v, float* red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    float incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        float n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    __syncthreads();
+    if (lane == 31) red[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        float s = lane < nw ? red[lane] : 0.f;
+        float si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            float n = __shfl_up_sync(0xFFFFFFFFu, si, o);
+            if (lane >= o) si += n;
+        }
+        if (lane < nw) red[lane] = si - s;
+    }
+    __syncthreads();
+    float r = red[wid] + incl;
+    __syncthreads();
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// order-preserving uint32 keys of floats (-0 folded into +0, NaN to -inf)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t float_key(float f) {
+    if (f != f) f = -INFINITY;
+    f = f + 0.0f;
+    uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+    uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+    return __uint_as_float(b);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + 1-D bulk async copy (TMA engine), with bounded waits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for the phase with the given parity; gives up after kWaitLimitNs and
+// returns false (the caller records an error and stops issuing work).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+// Global -> shared bulk copy, completion signalled on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+}  // namespace ekv

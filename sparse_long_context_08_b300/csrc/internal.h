@@ -1,0 +1,113 @@
+// Host-side interfaces between the C ABI (abi.cu) and the kernel translation
+// units (meta.cu, score.cu, select.cu, decode.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ekv {
+
+// A paged KV cache, already validated on the host (see entmaxkv.h for layouts).
+struct KV {
+    const void*    k;
+    const void*    v;
+    int            dtype;      // 0 fp32, 1 bf16
+    int            nb;         // num_blocks
+    int            hkv;        // num_kv_heads
+    int            P;          // page_size
+    int            D;          // head_dim
+    const int32_t* pt;         // page_table [B, maxp]
+    int            maxp;       // max_pages
+    const int32_t* sl;         // seq_lens [B]
+    int            B;          // batch
+};
+
+// Workspace of one decode call, carved from the caller's buffer.  U = B * Hkv
+// units (sequence, kv head); each unit's union of selected pages is split into
+// chunks of CH pages, one CTA per chunk.
+struct DecodeLayout {
+    int    U, G, Umax, CH, Smax, zcap;
+    size_t union_count, head_count, counter, vpages, union_page, union_mask, union_rank;
+    size_t z, tau, partial, total;
+};
+DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap);
+
+cudaError_t launch_build_meta(const KV& kv, int first_page, int num_pages, void* kmin,
+                              void* kmax, float* mean, float* var, bool bbox, bool gauss,
+                              cudaStream_t s);
+cudaError_t launch_score(const float* q, int Hq, float scale, const KV& kv, const void* kmin,
+                         const void* kmax, const float* mean, const float* var, int policy,
+                         float* out, cudaStream_t s);
+cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp, int32_t* sel,
+                               int32_t* n_sel, float* aux, cudaStream_t s);
+cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, float alpha,
+                                float delta, int32_t* sel, int32_t* n_sel, float* aux,
+                                cudaStream_t s);
+cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, const int32_t* sel,
+                          const int32_t* n_sel, int cap, float alpha, float* out, float* tau_out,
+                          int32_t* support_out, void* ws, const DecodeLayout& L, cudaStream_t s);
+
+// Optional events recorded between the decode kernels (plan | qk | tau | pv):
+// events[0] before plan, [1] before qk, [2] before tau, [3] before pv,
+// [4] after pv.  n = 0 disables.  Process-wide; for measurement only.
+void set_decode_stage_events(const cudaEvent_t* events, int n);
+
+// Per-unit counters of the last decode that used this workspace: union pages
+// whose K was read, and pages whose V was read.
+cudaError_t read_decode_counts(const void* ws, const DecodeLayout& L, int32_t* union_pages,
+                               int32_t* v_pages, cudaStream_t s);
+
+// Sticky device-data check words, one per translation unit: read, OR'd into
+// *flag, and cleared.
+cudaError_t take_status_meta(int* flag, cudaStream_t s);
+cudaError_t take_status_score(int* flag, cudaStream_t s);
+cudaError_t take_status_select(int* flag, cudaStream_t s);
+cudaError_t take_status_decode(int* flag, cudaStream_t s);
+
+// Limits of the selection kernels (pages held in shared memory per head).
+constexpr int kMaxPagesTopk = 49152;
+constexpr int kMaxPagesGauss = 12288;
+
+}  // namespace ekv
+
+// Per-TU definition of the status word and its host accessor.
+#define EKV_DEFINE_STATUS(NAME)                                                        \
+    namespace ekv {                                                                    \
+    static __device__ int g_status_word;                                               \
+    __device__ __forceinline__ void flag_bad_data() { atomicOr(&g_status_word, 1); }  \
+    cudaError_t take_status_##NAME(int* flag, cudaStream_t s) {                        \
+        int v = 0;                                                                     \
+        cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_status_word, sizeof(int), 0,   \
+                                                  cudaMemcpyDeviceToHost, s);          \
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);                            \
+        if (e != cudaSuccess) return e;                                                \
+        if (v) {                                                                       \
+            static const int zero = 0;                                                 \
+            e = cudaMemcpyToSymbolAsync(g_status_word, &zero, sizeof(int), 0,          \
+                                        cudaMemcpyHostToDevice, s);                    \
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);                        \
+            *flag |= 1;                                                                \
+        }                                                                              \
+        return e;                                                                      \
+    }                                                                                  \
+    }
+
+// Compile-time dispatch over the supported (dtype, head_dim, group) shapes.
+#define EKV_DISPATCH_D(D_, ...)                          \
+    switch (D_) {                                        \
+        case 64: { constexpr int kD = 64; __VA_ARGS__; } break;   \
+        case 128: { constexpr int kD = 128; __VA_ARGS__; } break; \
+        default: return cudaErrorInvalidValue;           \
+    }
+#define EKV_DISPATCH_G(G_, ...)                          \
+    switch (G_) {                                        \
+        case 1: { constexpr int kG = 1; __VA_ARGS__; } break; \
+        case 2: { constexpr int kG = 2; __VA_ARGS__; } break; \
+        case 4: { constexpr int kG = 4; __VA_ARGS__; } break; \
+        case 8: { constexpr int kG = 8; __VA_ARGS__; } break; \
+        default: return cudaErrorInvalidValue;           \
+    }
+#define EKV_DISPATCH_T(DT_, ...)                         \
+    if ((DT_) == 1) { using T = ::ekv::bf16raw; __VA_ARGS__; } \
+    else { using T = float; __VA_ARGS__; }

@@ -1,0 +1,348 @@
+// Candidate page selection [EntmaxKV §2.B].
+//
+// Top-k (§2.B.1): one CTA per (sequence, query head) holds the head's page
+// bounds as order-preserving uint32 keys in shared memory, finds the k-th
+// largest key with a 4-pass MSB radix select (8-bit digits, per-warp
+// histograms), then writes the selected pages in ascending order with two
+// block scans: ties at the k-th key go to the lower page ids.
+//
+// Gaussian tau-hat (§2.B.2): one CTA per (sequence, query head) solves
+//   F(tau) = sum_p n_p E[((alpha-1) X_p - tau)_+^e] - 1 = 0,  X_p ~ N(m_p, s_p^2)
+// with a safeguarded Newton iteration from tau = max_p (alpha-1) m_p - 1
+// (F >= 0 there; F is convex and decreasing, so Newton climbs monotonically),
+// keeps pages whose (alpha-1) * estimated max clears tau-hat - delta, and caps
+// the kept set by estimated-max rank with the same radix select.
+#include "common.cuh"
+
+EKV_DEFINE_STATUS(select)
+
+namespace ekv {
+
+constexpr int kSelThreads = 1024;
+
+struct SelShared {
+    int red[40];
+    uint32_t ured[32];
+    int digit, above;
+};
+
+// k-th largest key among keys[0..n) (1 <= k <= n) and how many entries equal
+// to it are taken (the rest being strictly larger).  whist: [warps][256] ints.
+__device__ void radix_kth(const uint32_t* keys, int n, int k, int* whist, int* hist,
+                          SelShared& sh, uint32_t& kth, int& take_eq) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nw = blockDim.x >> 5;
+    uint32_t prefix = 0, pmask = 0;
+    int rem = k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < nw * 256; i += blockDim.x) whist[i] = 0;
+        __syncthreads();
+        int* mine = whist + wid * 256;
+        for (int i = tid; i < n; i += blockDim.x) {
+            const uint32_t key = keys[i];
+            if ((key & pmask) == prefix) atomicAdd(&mine[(key >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        for (int d = tid; d < 256; d += blockDim.x) {
+            int s = 0;
+            for (int w = 0; w < nw; ++w) s += whist[w * 256 + d];
+            hist[d] = s;
+        }
+        __syncthreads();
+        if (wid == 0) {
+            int lsum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) lsum += hist[lane * 8 + j];
+            // exclusive suffix sum over lanes (buckets above this lane's)
+            int incl = lsum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+                if (lane + o < 32) incl += v;
+            }
+            int acc = incl - lsum;
+#pragma unroll
+            for (int j = 7; j >= 0; --j) {
+                const int d = lane * 8 + j;
+                const int c = hist[d];
+                if (acc < rem && acc + c >= rem) { sh.digit = d; sh.above = acc; }
+                acc += c;
+            }
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(sh.digit) << shift;
+        pmask |= 255u << shift;
+        rem -= sh.above;
+        __syncthreads();
+    }
+    kth = prefix;
+    take_eq = rem;
+}
+
+// Writes, in ascending index order, every i with keys[i] > kth plus the first
+// take_eq indices with keys[i] == kth.  Returns the count; *next_key receives
+// the largest key not taken (0 if all were taken).
+__device__ int compact_topk(const uint32_t* keys, int n, uint32_t kth, int take_eq,
+                            int32_t* dst, SelShared& sh, uint32_t* next_key) {
+    const int tid = threadIdx.x;
+    const int seg = (n + blockDim.x - 1) / blockDim.x;
+    const int i0 = min(n, tid * seg), i1 = min(n, i0 + seg);
+    int eq = 0;
+    for (int i = i0; i < i1; ++i) eq += keys[i] == kth;
+    int tot;
+    int eq_rank = block_exclusive_scan(eq, sh.red, &tot);
+    int cnt = 0;
+    uint32_t best_out = 0;
+    {
+        int r = eq_rank;
+        for (int i = i0; i < i1; ++i) {
+            const uint32_t key = keys[i];
+            bool take = key > kth;
+            if (key == kth) { take = r < take_eq; ++r; }
+            if (take) ++cnt; else best_out = max(best_out, key);
+        }
+    }
+    int pos = block_exclusive_scan(cnt, sh.red, &tot);
+    {
+        int r = eq_rank;
+        for (int i = i0; i < i1; ++i) {
+            const uint32_t key = keys[i];
+            bool take = key > kth;
+            if (key == kth) { take = r < take_eq; ++r; }
+            if (take) dst[pos++] = i;
+        }
+    }
+    *next_key = block_max_u(best_out, sh.ured);
+    return tot;
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
+                   int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
+                   float* __restrict__ aux) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ SelShared sh;
+    const int nw = blockDim.x >> 5;
+    int* whist = reinterpret_cast<int*>(smem_raw);
+    int* hist = whist + nw * 256;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(hist + 256);
+
+    const int bh = blockIdx.x;
+    const int b = bh / Hq;
+    const int len = kv.sl[b];
+    const int np = min(kv.maxp, (len + kv.P - 1) / kv.P);
+    const float* src = bound + (int64_t)bh * kv.maxp;
+    int32_t* dst = sel + (int64_t)bh * kp;
+    for (int i = threadIdx.x; i < np; i += blockDim.x) keys[i] = float_key(src[i]);
+    __syncthreads();
+    const int k = min(kp, np);
+    if (k <= 0) {
+        if (threadIdx.x == 0) {
+            n_sel[bh] = 0;
+            if (aux) { aux[2 * bh] = INFINITY; aux[2 * bh + 1] = -INFINITY; }
+        }
+        return;
+    }
+    uint32_t kth;
+    int take_eq;
+    if (k == np) {
+        kth = 0;              // below every real key: take everything
+        take_eq = 0;
+    } else {
+        radix_kth(keys, np, k, whist, hist, sh, kth, take_eq);
+    }
+    uint32_t next_key;
+    const int got = compact_topk(keys, np, kth, take_eq, dst, sh, &next_key);
+    if (threadIdx.x == 0) {
+        n_sel[bh] = got;
+        if (aux) {
+            float kth_f = INFINITY;
+            if (k == np) {
+                // smallest kept bound when every page is kept
+                kth_f = INFINITY;
+            } else {
+                kth_f = key_float(kth);
+            }
+            aux[2 * bh] = kth_f;
+            aux[2 * bh + 1] = k < np ? key_float(next_key) : -INFINITY;
+        }
+    }
+    if (k == np && aux) {
+        // every page kept: the smallest kept bound is the minimum key
+        uint32_t mn = 0xFFFFFFFFu;
+        for (int i = threadIdx.x; i < np; i += blockDim.x) mn = min(mn, keys[i]);
+        const uint32_t mx = block_max_u(~mn, sh.ured);
+        if (threadIdx.x == 0) aux[2 * bh] = key_float(~mx);
+    }
+}
+
+// E[(Y - tau)_+^e] and its derivative magnitude -dE/dtau for Y ~ N(mu, sig^2):
+//   e = 2: E = (a^2 + sig^2) Phi(u) + a sig phi(u),   -dE = 2 (a Phi(u) + sig phi(u))
+//   e = 1: E = a Phi(u) + sig phi(u),                  -dE = Phi(u)
+// with a = mu - tau, u = a / sig; sig = 0 gives (a)_+^e.
+template <int E>
+__device__ __forceinline__ float2 gauss_moment(float mu, float sig, float tau) {
+    const float a = mu - tau;
+    if (!(sig > 0.f)) {
+        const float ap = fmaxf(a, 0.f);
+        return E == 2 ? make_float2(ap * ap, 2.f * ap) : make_float2(ap, a > 0.f ? 1.f : 0.f);
+    }
+    const float u = a / sig;
+    const float Phi = 0.5f * erfcf(-u * 0.70710678118654752f);
+    const float phi = 0.39894228040143268f * expf(-0.5f * u * u);
+    const float m1 = fmaf(a, Phi, sig * phi);
+    if (E == 2) return make_float2(fmaf(fmaf(a, a, sig * sig), Phi, a * sig * phi), 2.f * m1);
+    return make_float2(m1, Phi);
+}
+
+template <int E>
+__global__ void __launch_bounds__(kSelThreads)
+select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float alpha,
+                    float delta, int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
+                    float* __restrict__ aux) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ SelShared sh;
+    __shared__ float2 fred[32];
+    __shared__ float fmaxred[32];
+    const int nw = blockDim.x >> 5;
+    int* whist = reinterpret_cast<int*>(smem_raw);
+    int* hist = whist + nw * 256;
+    const int np_max = kv.maxp;
+    float* s_mu = reinterpret_cast<float*>(hist + 256);
+    float* s_sg = s_mu + np_max;
+    float* s_n = s_sg + np_max;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(s_n + np_max);
+
+    const int bh = blockIdx.x;
+    const int b = bh / Hq;
+    const int len = kv.sl[b];
+    const int np = min(kv.maxp, (len + kv.P - 1) / kv.P);
+    const float c = alpha - 1.f;
+    const float* src = ms + (int64_t)bh * kv.maxp * 2;
+    float mu_max = -INFINITY;
+    for (int p = threadIdx.x; p < np; p += blockDim.x) {
+        const float m = src[2 * p], s = src[2 * p + 1];
+        const int n = min(kv.P, len - p * kv.P);
+        const float zmax = n > 1 ? fmaf(sqrtf(2.f * logf(static_cast<float>(n))), s, m) : m;
+        s_mu[p] = c * m;
+        s_sg[p] = c * s;
+        s_n[p] = static_cast<float>(n);
+        keys[p] = float_key(zmax);
+        mu_max = fmaxf(mu_max, c * m);
+    }
+    mu_max = block_max(mu_max, fmaxred);
+    if (np <= 0) {
+        if (threadIdx.x == 0) {
+            n_sel[bh] = 0;
+            if (aux) { aux[2 * bh] = INFINITY; aux[2 * bh + 1] = 0.f; }
+        }
+        return;
+    }
+
+    // safeguarded Newton on the convex, decreasing F
+    float lo = mu_max - 1.f, hi = INFINITY, tau = lo;
+    for (int it = 0; it < 64; ++it) {
+        float2 acc = make_float2(0.f, 0.f);
+        for (int p = threadIdx.x; p < np; p += blockDim.x) {
+            const float2 v = gauss_moment<E>(s_mu[p], s_sg[p], tau);
+            acc.x = fmaf(s_n[p], v.x, acc.x);
+            acc.y = fmaf(s_n[p], v.y, acc.y);
+        }
+        acc = block_sum2(acc, fred);
+        const float F = acc.x - 1.f, dF = acc.y;
+        if (F == 0.f) break;                       // tau is the root
+        if (F > 0.f) lo = tau; else hi = tau;
+        const float tol = 1e-7f * fmaxf(1.f, fabsf(tau));
+        if (dF > 0.f) {
+            const float nxt = tau + F / dF;
+            if (fabsf(nxt - tau) <= tol) {         // converged (to fp32 resolution)
+                if (nxt > lo && nxt < hi) tau = nxt;
+                break;
+            }
+            if (nxt > lo && nxt < hi) { tau = nxt; continue; }
+        }
+        if (hi < INFINITY) {
+            if (hi - lo <= tol) break;
+            tau = 0.5f * (lo + hi);                // safeguard: bisect the bracket
+        } else {
+            tau = lo + fmaxf(1.f, 2.f * (lo - (mu_max - 1.f)));   // no upper end yet: expand
+        }
+    }
+    const float tau_hat = tau;
+
+    // threshold test; the uint32 key of a page that fails is 0 (below all)
+    int pass = 0;
+    for (int p = threadIdx.x; p < np; p += blockDim.x) {
+        const float zmax = key_float(keys[p]);
+        const bool ok = c * zmax >= tau_hat - delta;
+        pass += ok;
+        if (!ok) keys[p] = 0u;
+    }
+    pass = block_sum_i(pass, sh.red);
+    int32_t* dst = sel + (int64_t)bh * cap;
+    uint32_t kth = 1u;   // every passing page has a key >= 1
+    int take_eq = 0;
+    if (pass > cap) {
+        radix_kth(keys, np, cap, whist, hist, sh, kth, take_eq);
+    } else if (pass == 0) {
+        // no page clears the threshold: keep the argmax estimated max (lowest id)
+        for (int p = threadIdx.x; p < np; p += blockDim.x) {
+            const int n = min(kv.P, len - p * kv.P);
+            const float m = src[2 * p], s = src[2 * p + 1];
+            keys[p] = float_key(n > 1 ? fmaf(sqrtf(2.f * logf(static_cast<float>(n))), s, m) : m);
+        }
+        radix_kth(keys, np, 1, whist, hist, sh, kth, take_eq);
+    }
+    uint32_t next_key;
+    const int got = compact_topk(keys, np, kth, take_eq, dst, sh, &next_key);
+    if (threadIdx.x == 0) {
+        n_sel[bh] = got;
+        if (aux) { aux[2 * bh] = tau_hat; aux[2 * bh + 1] = static_cast<float>(pass); }
+    }
+}
+
+static int max_optin_smem() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 48 * 1024;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return 48 * 1024;
+    return v;
+}
+
+cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp, int32_t* sel,
+                               int32_t* n_sel, float* aux, cudaStream_t s) {
+    const int threads = kSelThreads;
+    const size_t smem = (size_t)(threads / 32) * 256 * 4 + 256 * 4 + (size_t)kv.maxp * 4;
+    if ((int)smem > max_optin_smem() - (int)sizeof(SelShared)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    select_topk_kernel<<<kv.B * Hq, threads, smem, s>>>(bound, kv, Hq, kp, sel, n_sel, aux);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, float alpha,
+                                float delta, int32_t* sel, int32_t* n_sel, float* aux,
+                                cudaStream_t s) {
+    const int threads = kSelThreads;
+    const size_t smem = (size_t)(threads / 32) * 256 * 4 + 256 * 4 + (size_t)kv.maxp * 16;
+    if ((int)smem > max_optin_smem() - 1024) return cudaErrorInvalidValue;
+    const bool e2 = fabsf(alpha - 1.5f) < 1e-6f;
+    cudaError_t e;
+    if (e2) {
+        e = cudaFuncSetAttribute(select_gauss_kernel<2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        select_gauss_kernel<2><<<kv.B * Hq, threads, smem, s>>>(ms, kv, Hq, cap, alpha, delta,
+                                                                 sel, n_sel, aux);
+    } else {
+        e = cudaFuncSetAttribute(select_gauss_kernel<1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        select_gauss_kernel<1><<<kv.B * Hq, threads, smem, s>>>(ms, kv, Hq, cap, alpha, delta,
+                                                                 sel, n_sel, aux);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ekv

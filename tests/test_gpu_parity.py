@@ -1,0 +1,233 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, stage by
+stage, on seeded workloads that span several tiles and ragged tails, plus the
+edge cases the method has.  Tolerances: tests/gpu_util.py."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_long_context_08_b300 import entmaxkv as E
+from sparse_long_context_08_b300.workloads import make_workload
+
+from gpu_util import (GpuRun, bbox_scale, compare_decode, compare_meta, compare_scores,
+                      compare_selection, gauss_scale)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from sparse_long_context_08_b300 import build
+    build.build()
+    oracle.lib()
+
+
+def full_parity(w, heads=None, check_e2e=True):
+    """Every stage of one decode step against the oracle; returns report dict."""
+    g = GpuRun(w)
+    r = g.step()
+    kv = oracle.KV(w)
+    om = oracle.build_meta(kv)
+    compare_meta(w, g.meta(), om)
+    BH = w.batch * w.num_q_heads
+    hs = list(range(BH)) if heads is None else list(heads)
+    s = float(w.scale)
+    rep = {}
+    if w.policy == "topk":
+        ob = oracle.score_bbox(kv, om, s, heads=hs)
+        mag = bbox_scale(w, om, hs)
+        compare_scores(w, r["page_scores"], ob, mag, hs)
+        osel, on, okth, onext = oracle.select_topk(kv, ob, w.cap_pages, heads=hs)
+        rep["ties"] = compare_selection(w, r["sel"], r["n_sel"], osel, on, ob, mag, okth, hs)
+        for bh in hs:
+            assert r["n_sel"][bh] == on[bh]
+            if on[bh] < w.pages_of(bh // w.num_q_heads):
+                assert abs(r["aux"][bh, 0] - okth[bh]) <= 1e-5 * mag[bh].max()
+    else:
+        om_, os_ = oracle.score_gauss(kv, om, s, heads=hs)
+        mag = gauss_scale(w, om, hs)
+        compare_scores(w, r["page_scores"][..., 0], om_, mag, hs)
+        compare_scores(w, r["page_scores"][..., 1], os_, mag, hs)
+        osel, on, oth, ozmax = oracle.select_gauss(kv, om_, os_, w.alpha, w.delta, w.cap_pages,
+                                                   heads=hs)
+        for bh in hs:
+            assert abs(r["aux"][bh, 0] - oth[bh]) <= 1e-5 * max(1.0, abs(oth[bh])), \
+                (bh, r["aux"][bh, 0], oth[bh])
+        # the decision score is (alpha-1) zmax against tau-hat - delta, or the
+        # cap's k-th zmax; report either kind of boundary tie
+        c = w.alpha - 1.0
+        zs = c * ozmax
+        bnd = np.full(BH, np.nan)
+        for bh in hs:
+            np_ = w.pages_of(bh // w.num_q_heads)
+            passing = np.sort(zs[bh, :np_][zs[bh, :np_] >= oth[bh] - w.delta])[::-1]
+            bnd[bh] = passing[w.cap_pages - 1] if len(passing) > w.cap_pages else oth[bh] - w.delta
+        rep["ties"] = compare_selection(w, r["sel"], r["n_sel"], osel, on, zs, c * mag, bnd, hs)
+    # decode on the oracle's own selection
+    g_out, g_tau, g_sup = g.decode_with(osel, on)
+    o_out, o_tau, o_sup, o_psum = oracle.decode_sparse(kv, s, w.alpha, osel, on, heads=hs)
+    compare_decode(g_out, g_tau, o_out, o_tau, hs, g_sup, o_sup)
+    # end to end: where the two selections agree, the outputs agree
+    if check_e2e:
+        same = [bh for bh in hs if r["n_sel"][bh] == on[bh]
+                and np.array_equal(r["sel"][bh, :on[bh]], osel[bh, :on[bh]])]
+        assert len(same) >= 0.9 * len(hs)
+        compare_decode(r["out"], r["tau"], o_out, o_tau, same)
+    assert E.entmaxkv_read_device_status() == E.EKV_OK
+    rep["support"] = o_sup
+    return rep
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at oracle-friendly sizes (ragged tails included)
+# ---------------------------------------------------------------------------
+
+def test_tiny_full_size():
+    full_parity(make_workload("tiny"))
+
+
+def test_tiny_ragged_tail():
+    full_parity(make_workload("tiny", seq_lens=[4096 - 7], context=4089))
+
+
+def test_gqa_reduced_context_ragged():
+    full_parity(make_workload("gqa32k", batch=2, seq_lens=[8192, 5000]))
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_long128k_reduced(alpha):
+    full_parity(make_workload("long128k", batch=2, seq_lens=[16384, 12345], alpha=alpha))
+
+
+def test_ctx1m_reduced():
+    full_parity(make_workload("ctx1m", context=65536))
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_gauss_reduced(alpha):
+    full_parity(make_workload("gauss64k", batch=2, seq_lens=[16384, 9999], alpha=alpha))
+
+
+# ---------------------------------------------------------------------------
+# shapes: head_dim, dtype, group size, page size, general alpha
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (8, 1)])
+def test_shapes(d, dtype, hq, hkv):
+    w = make_workload("long128k", batch=2, seq_lens=[3000, 2049], head_dim=d, dtype=dtype,
+                      num_q_heads=hq, num_kv_heads=hkv, page_size=16, budget_tokens=512,
+                      planted_pages=4, seed=100 + d + hq * hkv)
+    full_parity(w)
+
+
+@pytest.mark.parametrize("alpha", [1.3, 2.5])
+def test_general_alpha_bisection(alpha):
+    full_parity(make_workload("long128k", batch=1, context=8192, alpha=alpha, seed=7))
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+def test_budget_covers_every_page_and_single_page_sequences():
+    w = make_workload("long128k", batch=3, seq_lens=[5 * 32, 20, 1], budget_tokens=4096,
+                      planted_pages=0)
+    rep = full_parity(w)
+    g = GpuRun(w)
+    r = g.step()
+    for bh in range(w.batch * w.num_q_heads):
+        np_ = w.pages_of(bh // w.num_q_heads)
+        assert list(r["sel"][bh, :r["n_sel"][bh]]) == list(range(np_))
+        assert r["aux"][bh, 1] == -np.inf
+
+
+def test_empty_selection_gives_zero_output():
+    w = make_workload("long128k", batch=1, context=2048)
+    g = GpuRun(w)
+    g.step()
+    BH = w.num_q_heads
+    sel = np.zeros((BH, w.cap_pages), np.int32)
+    n = np.zeros(BH, np.int32)
+    n[::2] = 3
+    sel[:, :3] = [0, 5, 9]
+    out, tau, sup = g.decode_with(sel, n)
+    kv = oracle.KV(w)
+    o_out, o_tau, o_sup, _ = oracle.decode_sparse(kv, float(w.scale), w.alpha, sel, n)
+    compare_decode(out, tau, o_out, o_tau, range(BH))
+    assert np.all(out[1::2] == 0) and np.all(np.isinf(tau[1::2])) and np.all(sup[1::2] == 0)
+
+
+def test_tie_storm_constant_keys():
+    """All keys equal: every bound ties (lowest pages win) and every kept token
+    gets the same weight, so out is the mean of the kept values."""
+    w = make_workload("long128k", batch=1, context=32 * 40, planted_pages=0, budget_tokens=32 * 7)
+    w.k_pool[:] = w.k_pool[0, 0, 0]
+    g = GpuRun(w)
+    r = g.step()
+    kv = oracle.KV(w)
+    for bh in range(w.num_q_heads):
+        assert list(r["sel"][bh, :r["n_sel"][bh]]) == list(range(7))
+    o_out, o_tau, o_sup, _ = oracle.decode_sparse(kv, float(w.scale), w.alpha, r["sel"], r["n_sel"])
+    compare_decode(r["out"], r["tau"], o_out, o_tau, range(w.num_q_heads))
+    assert np.all(r["support"] == 7 * 32)
+
+
+def test_sparsemax_single_token_support():
+    """alpha = 2 with one dominant key per head: the support is that token and
+    out equals its value row."""
+    w = make_workload("long128k", batch=1, context=4096, alpha=2.0, planted_pages=0,
+                      num_q_heads=8, num_kv_heads=8, head_dim=64, dtype="f32", seed=9)
+    # plant one key per head: 20 q/|q| at page 3, token 5
+    blk = w.page_table[0, 3]
+    for h in range(8):
+        qn = w.q[0, h] / np.linalg.norm(w.q[0, h])
+        w.k_pool[blk, h, 5] = 40.0 * qn
+    g = GpuRun(w)
+    r = g.step()
+    assert np.all(r["support"] == 1)
+    for h in range(8):
+        np.testing.assert_allclose(r["out"][h], w.v_pool[blk, h, 5], rtol=1e-6, atol=1e-6)
+    full_parity(w)
+
+
+def test_bad_page_table_entry_is_flagged_not_faulted():
+    w = make_workload("long128k", batch=1, context=2048, planted_pages=0)
+    w.page_table[0, 10] = w.num_blocks + 5     # out of range
+    g = GpuRun(w)
+    g.step()
+    assert E.entmaxkv_read_device_status() == E.EKV_DEVICE_CHECK_FAILED
+    assert E.entmaxkv_read_device_status() == E.EKV_OK     # read clears it
+
+
+def test_deterministic_across_runs():
+    w = make_workload("long128k", batch=2, context=8192)
+    g = GpuRun(w)
+    a = g.step()
+    b = g.step()
+    for k in ("page_scores", "sel", "n_sel", "out", "tau", "support"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_graph_capture_replays_the_step():
+    w = make_workload("long128k", batch=2, context=8192)
+    g = GpuRun(w)
+    ref = g.step()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g.dec.step(g.q)          # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.dec.step(g.q)
+    g.dec.out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    out = g.dec.out.cpu().numpy().astype(np.float64).reshape(ref["out"].shape)
+    assert np.array_equal(out, ref["out"])

@@ -91,7 +91,11 @@ double oracle_gauss_F(const double* m, const double* s, const int32_t* n, int np
 /* [EntmaxKV §2.B.2] tau-hat from F = 0 by bisection; keep page p iff
  * (alpha-1) zmax_p >= tau_hat - delta, zmax_p = m_p + sqrt(2 ln n_p) s_p;
  * more than cap -> the cap pages with the largest zmax (ties: lower page);
- * none -> the argmax page.  sel ascending.  zmax (optional) receives zmax_p. */
+ * none -> the argmax page.  sel ascending.  zmax (optional) receives zmax_p.
+ * The page prints no formula for tau-hat or the estimated maximum, so these
+ * are readings: parity unpinned against the page's own rule (the reading is
+ * pinned to its definition by quadrature, root finding and the zero-variance
+ * reduction in the tests). */
 int oracle_select_gauss(const oracle_kv* kv, int num_q_heads, const double* m,
                         const double* s, double alpha, double delta, int cap,
                         const int32_t* heads, int n_heads, int32_t* sel,

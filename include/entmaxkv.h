@@ -154,6 +154,34 @@ int entmaxkv_decode(const float* q, int32_t num_q_heads, float scale,
                     float* out, float* tau_out, int32_t* support_out,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* Bytes of the scratch array built into the library for
+ * entmaxkv_decode_noalloc. */
+#define ENTMAXKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* Stage 4 without a caller-provided workspace.  The page has no counterpart of
+ * this call; it exists for callers that cannot allocate device memory at the
+ * point where they decode (code running inside an allocator callback, a plugin
+ * that is handed only its input and output buffers, a server whose device
+ * memory is fixed before it starts taking requests).  Same arguments, results
+ * and checks as entmaxkv_decode, minus `workspace`/`ws_bytes`: the scratch is a
+ * fixed array of ENTMAXKV_NOALLOC_SCRATCH_BYTES inside the library, one per
+ * device that loads it, kept until the process exits.  It never allocates or
+ * frees memory.
+ * - Sizes whose workspace (entmaxkv_workspace_size) exceeds that array return
+ *   EKV_WORKSPACE_TOO_SMALL and launch nothing.
+ * - The first call on a device looks up the array's device address (with that
+ *   device current) and caches it; make that first call before any stream
+ *   capture.
+ * - All calls on a device share the one array, which keeps whatever the last
+ *   call left in it (each call re-initialises what it needs): calls whose work
+ *   can overlap on the GPU (other streams, other host threads) race and must
+ *   be serialised by the caller. */
+int entmaxkv_decode_noalloc(const float* q, int32_t num_q_heads, float scale,
+                            const ekv_paged_kv* kv, const int32_t* sel,
+                            const int32_t* n_sel, int32_t cap_pages, float alpha,
+                            float* out, float* tau_out, int32_t* support_out,
+                            void* stream);
+
 /* Host-only: bytes of workspace entmaxkv_decode needs for these sizes
  * (0 if the sizes are invalid). */
 size_t entmaxkv_workspace_size(int32_t batch, int32_t num_q_heads,

@@ -30,7 +30,7 @@ EKV_SELECT_GAUSS = 1
 SYMBOLS = ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select",
            "entmaxkv_decode", "entmaxkv_workspace_size", "entmaxkv_status_string",
            "entmaxkv_read_device_status", "entmaxkv_version", "entmaxkv_set_stage_events",
-           "entmaxkv_decode_counts")
+           "entmaxkv_decode_counts", "entmaxkv_decode_noalloc")
 
 
 class EntmaxKVError(RuntimeError):
@@ -78,7 +78,7 @@ def lib() -> C.CDLL:
         L.entmaxkv_decode_counts.argtypes = [vp] + [i32] * 7 + [vp, vp, vp]
         for name in ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select",
                      "entmaxkv_decode", "entmaxkv_read_device_status",
-                     "entmaxkv_set_stage_events", "entmaxkv_decode_counts"):
+                     "entmaxkv_set_stage_events", "entmaxkv_decode_counts", "entmaxkv_decode_noalloc"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib

@@ -86,7 +86,7 @@ def workload_config(w):
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "alpha": w.alpha, "policy": w.policy,
             "budget_tokens": w.budget_tokens, "kv_dtype": w.dtype, "seed": w.seed,
-            "l2": "inputs (4 GiB K/V) larger than L2, and L2 flushed between timed steps"}
+            "l2": "inputs (4 GiB K/V) larger than L2; L2 flushed between timed steps (512 MiB write, then 256 MiB read)"}
 
 
 # ---------------------------------------------------------------------------
@@ -236,13 +236,32 @@ def run_ours(args):
                           w.budget_tokens, w.delta)
     dec.build_meta()
     torch.cuda.synchronize()
+    # L2 flush between timed steps: write a buffer larger than L2, then read
+    # another one so that the written lines are evicted (and written back)
+    # before the next step rather than during it
     flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device="cuda")
+    flush_read = torch.ones(max(1, args.flush_mb // 2) << 20, dtype=torch.uint8, device="cuda")
+
+    def flush_l2(i):
+        flush.fill_(i & 255)
+        flush_read.sum(dtype=torch.int32)
     stream = torch.cuda.current_stream()
 
-    def step(evs=None):
-        if evs is None:
-            dec.step(q)
-            return
+    # the step is replayed as a CUDA graph; event-record nodes at the stage
+    # boundaries time score | select | plan | qk | tau | pv on the device
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)]
+    for x in evs:
+        x.record()             # materialise the events before capture
+    torch.cuda.synchronize()
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap_stream):
+        for _ in range(2):
+            dec.step(q)        # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(cap_stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap_stream):
         evs[0].record()
         dec.score(q)
         evs[1].record()
@@ -250,36 +269,32 @@ def run_ours(args):
         E.entmaxkv_set_stage_events(evs[2:7])
         dec.decode(q)
         E.entmaxkv_set_stage_events(None)
+    torch.cuda.synchronize()
 
     for i in range(max(3, args.warmup)):
-        step()
-        flush.fill_(i & 255)
+        graph.replay()
+        flush_l2(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
-    for e in ev:            # create the underlying events outside the timed region
-        for x in e:
-            x.record()
+    names = ["score", "select", "plan", "qk", "tau", "pv"]
+    stage = {n: [] for n in names}
+    total = []
     sampler = ClockSampler(bus_id_of(local_rank)) if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
     torch.cuda.synchronize()
     for i in range(K):
-        step(ev[i])
-        flush.fill_((i + 7) & 255)
+        graph.replay()
+        torch.cuda.synchronize()
+        t = [evs[j].elapsed_time(evs[j + 1]) for j in range(6)]
+        for n_, v in zip(names, t):
+            stage[n_].append(v)
+        total.append(evs[0].elapsed_time(evs[6]))
+        flush_l2(i + 7)                     # L2 flush between steps, outside the events
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
-    # per-step stage times (ms): score | select | plan | qk | tau | pv
-    names = ["score", "select", "plan", "qk", "tau", "pv"]
-    stage = {n: [] for n in names}
-    total = []
-    for e in ev:
-        t = [e[j].elapsed_time(e[j + 1]) for j in range(6)]
-        for n, v in zip(names, t):
-            stage[n].append(v)
-        total.append(e[0].elapsed_time(e[6]))
     t_sum = torch.tensor([sum(total)], dtype=torch.float64, device="cuda")
     if world > 1:
         dist.all_reduce(t_sum, op=dist.ReduceOp.MAX)
@@ -326,10 +341,11 @@ def run_ours(args):
         q_dev = torch.empty_like(q)
         for _ in range(3):
             dec.step_host(q_host, out_host, q_dev)
+            stream.synchronize()
         torch.cuda.synchronize()
         times = []
         for i in range(K):
-            flush.fill_(i & 255)
+            flush_l2(i)
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             dec.step_host(q_host, out_host, q_dev)

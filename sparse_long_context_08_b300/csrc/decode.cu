@@ -4,36 +4,52 @@
 // own pages; the unit reads the UNION of those pages once.
 //
 //   plan  (1 CTA per unit)      bitmaps of each head's pages -> union list in
-//                               ascending page order, per-page head mask and
-//                               each head's rank of the page.
-//   qk    (CH pages per CTA)    bulk-copies K pages (cp.async.bulk, mbarrier
-//                               pipeline) into shared memory; z' = (alpha-1)
-//                               s q.k for the G heads with fp32 FMA (G <= 8
-//                               rows are far too few for a tensor-core tile);
-//                               each head's scores land in its own list.
-//   tau   (1 CTA per head)      exact threshold: candidates z' > max - 1 are
-//                               sorted (bitonic, shared memory); the closed
-//                               form on the top-k prefix (alpha 2: sparsemax;
-//                               alpha 1.5: quadratic) picks tau, polished by
-//                               Newton steps on sum (z'-tau)_+^e = 1; other
-//                               alpha: bisection.
-//   pv    (CH pages per CTA)    p = (z' - tau)_+^(1/(alpha-1)); V pages with no
-//                               positive weight for any head are never read;
-//                               split-K partial sums, and the last CTA of the
-//                               unit (atomic ticket) merges them in a fixed
-//                               order: out = sum p v / sum p.  tau is global,
-//                               so the merge is a plain sum.
+//                               ascending page order with a per-page head mask;
+//                               resets the unit's per-call state.
+//   qk    (persistent, 1 CTA    the flattened union lists of all units are cut
+//          per SM)              into one contiguous range per CTA.  A producer
+//                               warp resolves page-table entries and bulk-copies
+//                               K pages (cp.async.bulk) into a ring of slots;
+//                               each consumer warp owns a fixed subset of the
+//                               slots and turns a page into z' = (alpha-1) s q.k
+//                               for the G heads with fp32 FMA (G <= 8 query rows
+//                               cannot fill a tensor-core tile), reduced across
+//                               lanes by a transposing butterfly.  Scores are
+//                               stored per unit in union order, -inf where a head
+//                               did not select the page; per-head maxima go out
+//                               through atomics.
+//   tau   (1 CTA per head)      candidates z' > max - 1 (all others have zero
+//                               weight) are compacted in index order; tau solves
+//                               sum (z' - tau)_+^(1/(alpha-1)) = 1 by Newton from
+//                               the left (alpha 1.5 and 2: the function is convex,
+//                               so the iterates rise monotonically to the root)
+//                               or by bisection (other alpha).  The pages holding
+//                               the support are marked in a per-unit bitmap.
+//   pv    (chunks of marked     V pages with no positive weight are never read.
+//          pages per CTA)       p = (z' - tau)_+^(1/(alpha-1)); out = sum p v /
+//                               sum p.  A unit whose support pages fit one CTA
+//                               writes out directly; otherwise the chunks' partial
+//                               sums are merged in a fixed order by the unit's
+//                               last CTA (tau is global, so the merge is a sum).
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 EKV_DEFINE_STATUS(decode)
 
 namespace ekv {
 
-constexpr int kChunkPages = 16;   // union pages per qk / pv CTA
-constexpr int kQkThreads = 256;
-constexpr int kPvThreads = 256;
-constexpr int kPlanThreads = 512;
+constexpr int kPlanThreads = 256;
+constexpr int kQkConsumers = 12;                       // consumer warps per qk CTA
+constexpr int kQkThreads = 32 * (kQkConsumers + 1);    // + one producer warp
+constexpr int kQkGroup = 16;                           // pages resolved per producer step
+constexpr int kQkMaxSlots = 48;
+constexpr int kQkSmemBudget = 220 * 1024;
+constexpr int kMaxUnits = 8192;                        // qk keeps a prefix over units in smem
 constexpr int kTauThreads = 512;
+constexpr int kPvThreads = 256;
+constexpr int kPvMaxChunk = 16;                        // support pages per pv CTA
+constexpr int kPvStageBytes = 128 * 1024;
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -42,21 +58,23 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, 
     L.U = B * Hkv;
     L.G = Hq / Hkv;
     L.Umax = std::min(L.G * cap, max_pages);
-    L.CH = kChunkPages;
-    L.Smax = (L.Umax + L.CH - 1) / L.CH;
-    L.zcap = cap * P;
+    L.nbw = (L.Umax + 31) / 32;
+    // chunk size of the value stage, sized for fp32 pages (the largest); bf16
+    // launches use chunks at least this large, hence never more of them
+    L.CHV = std::max(1, std::min(kPvMaxChunk, kPvStageBytes / (P * D * 4)));
+    L.SmaxV = (L.Umax + L.CHV - 1) / L.CHV;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
     L.union_count = take(sizeof(int) * L.U);
-    L.head_count = take(sizeof(int) * (size_t)B * Hq);
     L.counter = take(sizeof(int) * L.U);
     L.vpages = take(sizeof(int) * L.U);
+    L.head_max = take(sizeof(uint32_t) * (size_t)B * Hq);
     L.union_page = take(sizeof(int) * (size_t)L.U * L.Umax);
     L.union_mask = take(sizeof(int) * (size_t)L.U * L.Umax);
-    L.union_rank = take(sizeof(int) * (size_t)L.U * L.Umax * L.G);
-    L.z = take(sizeof(float) * (size_t)B * Hq * L.zcap);
+    L.supp = take(sizeof(uint32_t) * (size_t)L.U * L.nbw);
+    L.z = take(sizeof(float) * (size_t)L.U * L.G * L.Umax * P);
     L.tau = take(sizeof(float) * (size_t)B * Hq);
-    L.partial = take(sizeof(float) * (size_t)L.U * L.Smax * L.G * (D + 1));
+    L.partial = take(sizeof(float) * (size_t)L.U * L.SmaxV * L.G * (D + 1));
     L.total = o;
     return L;
 }
@@ -64,24 +82,23 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, 
 // Workspace views (device addresses).
 struct WS {
     int* union_count;
-    int* head_count;
     int* counter;
     int* vpages;
+    uint32_t* head_max;   // order-preserving keys of each head's max z'
     int* union_page;
     int* union_mask;
-    int* union_rank;
-    float* z;
+    uint32_t* supp;       // [U][nbw] union pages holding a positive weight
+    float* z;             // [U][G][Umax * P]
     float* tau;
     float* partial;
 };
 static WS ws_views(void* base, const DecodeLayout& L) {
     char* c = static_cast<char*>(base);
-    return WS{reinterpret_cast<int*>(c + L.union_count), reinterpret_cast<int*>(c + L.head_count),
-              reinterpret_cast<int*>(c + L.counter), reinterpret_cast<int*>(c + L.vpages),
-              reinterpret_cast<int*>(c + L.union_page),
-              reinterpret_cast<int*>(c + L.union_mask), reinterpret_cast<int*>(c + L.union_rank),
-              reinterpret_cast<float*>(c + L.z), reinterpret_cast<float*>(c + L.tau),
-              reinterpret_cast<float*>(c + L.partial)};
+    return WS{reinterpret_cast<int*>(c + L.union_count), reinterpret_cast<int*>(c + L.counter),
+              reinterpret_cast<int*>(c + L.vpages), reinterpret_cast<uint32_t*>(c + L.head_max),
+              reinterpret_cast<int*>(c + L.union_page), reinterpret_cast<int*>(c + L.union_mask),
+              reinterpret_cast<uint32_t*>(c + L.supp), reinterpret_cast<float*>(c + L.z),
+              reinterpret_cast<float*>(c + L.tau), reinterpret_cast<float*>(c + L.partial)};
 }
 
 __device__ __forceinline__ int pages_of(const KV& kv, int b) {
@@ -95,225 +112,566 @@ template <int G>
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(KV kv, int Hq, const int32_t* __restrict__ sel, const int32_t* __restrict__ n_sel,
             int cap, WS ws, DecodeLayout L) {
-    extern __shared__ __align__(16) uint32_t s_plan[];
+    extern __shared__ __align__(16) uint32_t s_bits[];   // [G][nwm]
     __shared__ int red[40];
     const int nwm = (kv.maxp + 31) / 32;
-    uint32_t* bits = s_plan;                                        // [G][nwm]
-    int* pre = reinterpret_cast<int*>(bits + (size_t)G * nwm);     // [G+1][nwm]
-
     const int u = blockIdx.x;
     const int b = u / kv.hkv;
-    const int kvh = u % kv.hkv;
+    const int kvh = u - b * kv.hkv;
     const int np = pages_of(kv, b);
     const int nw = (np + 31) / 32;
-    for (int i = threadIdx.x; i < G * nwm; i += blockDim.x) bits[i] = 0u;
+    const int tid = threadIdx.x;
+
+    for (int i = tid; i < G * nw; i += blockDim.x) {
+        const int h = i / nw;
+        s_bits[h * nwm + (i - h * nw)] = 0u;
+    }
+    // per-call state the later stages accumulate into
+    if (tid < G) ws.head_max[b * Hq + kvh * G + tid] = 0u;
+    for (int i = tid; i < L.nbw; i += blockDim.x) ws.supp[(int64_t)u * L.nbw + i] = 0u;
+    if (tid == 0) ws.counter[u] = 0;
     __syncthreads();
     for (int h = 0; h < G; ++h) {
         const int bh = b * Hq + kvh * G + h;
         int ns = n_sel[bh];
         if (ns < 0 || ns > cap) {
-            if (threadIdx.x == 0) flag_bad_data();
+            if (tid == 0) flag_bad_data();
             ns = max(0, min(ns, cap));
         }
-        for (int r = threadIdx.x; r < ns; r += blockDim.x) {
+        for (int r = tid; r < ns; r += blockDim.x) {
             const int p = sel[(int64_t)bh * cap + r];
-            if (p >= 0 && p < np) atomicOr(&bits[h * nwm + (p >> 5)], 1u << (p & 31));
+            if (p >= 0 && p < np) atomicOr(&s_bits[h * nwm + (p >> 5)], 1u << (p & 31));
             else flag_bad_data();
         }
     }
     __syncthreads();
 
     const int seg = (nw + blockDim.x - 1) / blockDim.x;
-    const int w0 = min(nw, threadIdx.x * seg), w1 = min(nw, w0 + seg);
-    int totals[G + 1];
+    const int w0 = min(nw, tid * seg), w1 = min(nw, w0 + seg);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) {
+        uint32_t x = 0;
 #pragma unroll
-    for (int a = 0; a <= G; ++a) {
-        int local = 0;
-        for (int w = w0; w < w1; ++w) {
-            uint32_t word = 0;
-            if (a < G) word = bits[a * nwm + w];
-            else
-#pragma unroll
-                for (int h = 0; h < G; ++h) word |= bits[h * nwm + w];
-            local += __popc(word);
-        }
-        int run = block_exclusive_scan(local, red, &totals[a]);
-        for (int w = w0; w < w1; ++w) {
-            uint32_t word = 0;
-            if (a < G) word = bits[a * nwm + w];
-            else
-#pragma unroll
-                for (int h = 0; h < G; ++h) word |= bits[h * nwm + w];
-            pre[a * nwm + w] = run;
-            run += __popc(word);
-        }
+        for (int h = 0; h < G; ++h) x |= s_bits[h * nwm + w];
+        cnt += __popc(x);
     }
-    if (threadIdx.x == 0) {
-        ws.union_count[u] = totals[G];
-        ws.counter[u] = 0;
-        ws.vpages[u] = 0;
-#pragma unroll
-        for (int h = 0; h < G; ++h) ws.head_count[b * Hq + kvh * G + h] = totals[h];
-    }
-    __syncthreads();
+    int total;
+    int idx = block_exclusive_scan(cnt, red, &total);
     int* upage = ws.union_page + (int64_t)u * L.Umax;
     int* umask = ws.union_mask + (int64_t)u * L.Umax;
-    int* urank = ws.union_rank + (int64_t)u * L.Umax * G;
     for (int w = w0; w < w1; ++w) {
         uint32_t hw[G];
         uint32_t uw = 0;
 #pragma unroll
-        for (int h = 0; h < G; ++h) { hw[h] = bits[h * nwm + w]; uw |= hw[h]; }
-        int idx = pre[G * nwm + w];
+        for (int h = 0; h < G; ++h) { hw[h] = s_bits[h * nwm + w]; uw |= hw[h]; }
         while (uw) {
             const int bit = __ffs(uw) - 1;
             uw &= uw - 1;
-            const uint32_t below = (1u << bit) - 1u;
             int mask = 0;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const bool in = (hw[h] >> bit) & 1u;
-                mask |= in ? (1 << h) : 0;
-                urank[(int64_t)idx * G + h] = in ? pre[h * nwm + w] + __popc(hw[h] & below) : -1;
-            }
+            for (int h = 0; h < G; ++h) mask |= static_cast<int>((hw[h] >> bit) & 1u) << h;
             upage[idx] = w * 32 + bit;
             umask[idx] = mask;
             ++idx;
         }
     }
+    if (tid == 0) ws.union_count[u] = total;
 }
 
 // ---------------------------------------------------------------------------
 // qk: scores of the union pages
 // ---------------------------------------------------------------------------
-template <int D, int G, typename T>
-struct QkShape {
-    static constexpr int EPC = Elem<T>::kPer16;
-    static constexpr int RC = D / EPC;                       // 16-byte chunks per key row
-    static constexpr int LPT0 = (G * D / 64) < 2 ? 2 : (G * D / 64);
-    static constexpr int LPT = LPT0 > RC ? RC : LPT0;       // lanes per token
-    static constexpr int CPL = RC / LPT;                     // chunks per lane
-    static constexpr int TPW = 32 / LPT;                     // tokens per warp pass
-    static constexpr int NW = kQkThreads / 32;
-    static constexpr int TPP = NW * TPW;                     // tokens per CTA pass
+template <typename T, int D, int G>
+struct QkCfg {
+    static constexpr int EPC = Elem<T>::kPer16;             // elements per 16-byte chunk
+    static constexpr int RC = D / EPC;                      // chunks per key row
+    static constexpr int C0 = (RC / G) < 2 ? (RC / G) : 2;
+    static constexpr int C1 = 64 / (G * EPC);               // keeps q at <= 64 registers
+    static constexpr int CPL = C1 < C0 ? C1 : C0;           // chunks per lane
+    static constexpr int LPT = RC / CPL;                    // lanes per token (>= G)
+    static constexpr int TPW = 32 / LPT;                    // tokens per warp pass
+    static constexpr int DUP = LPT / G;                     // lanes left holding each head's sum
+    static_assert(CPL >= 1 && LPT >= G && LPT <= 32, "unsupported qk shape");
 };
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kQkThreads)
-qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, DecodeLayout L,
-          int sp, int nstages) {
-    using S = QkShape<D, G, T>;
-    extern __shared__ __align__(128) unsigned char s_raw[];
-    __shared__ __align__(8) uint64_t bars[8];
-    __shared__ int s_blk[kChunkPages], s_valid[kChunkPages], s_mask[kChunkPages];
-    __shared__ int s_rank[kChunkPages][G];
-
-    const int u = blockIdx.y;
-    const int c = blockIdx.x;
-    const int ucnt = ws.union_count[u];
-    const int i0 = c * L.CH;
-    if (i0 >= ucnt) return;
-    const int npg = min(ucnt, i0 + L.CH) - i0;
-    const int b = u / kv.hkv;
-    const int kvh = u % kv.hkv;
-    const int P = kv.P;
-    const int len = kv.sl[b];
-    const int tid = threadIdx.x;
-
-    if (tid < npg) {
-        const int idx = u * L.Umax + i0 + tid;
-        const int page = ws.union_page[idx];
-        int blk = kv.pt[(int64_t)b * kv.maxp + page];
-        int valid = min(P, len - page * P);
-        if (blk < 0 || blk >= kv.nb) { flag_bad_data(); blk = 0; valid = 0; }
-        s_blk[tid] = blk;
-        s_valid[tid] = valid;
-        s_mask[tid] = ws.union_mask[idx];
+// Sums a[0..C) over the M*2 lanes of an aligned lane group, handing each
+// lane one head: at every level a lane keeps half of its values (the upper
+// half if its lane bit is set) and adds its partner's copy of that half, so
+// C values cost C-1 shuffles instead of C*log2(lanes).  On return a[0] holds
+// the complete sum of value index lt / (lanes / C) for lane-in-group lt.
+template <int C, int M>
+struct XReduce {
+    __device__ __forceinline__ static void run(float* a, int lt) {
+        if constexpr (M >= 1) {
+            if constexpr (C >= 2) {
+                constexpr int H = C / 2;
+                const bool up = (lt & M) != 0;
 #pragma unroll
-        for (int h = 0; h < G; ++h) s_rank[tid][h] = ws.union_rank[(int64_t)idx * G + h];
+                for (int j = 0; j < H; ++j) {
+                    const float send = up ? a[j] : a[j + H];
+                    const float keep = up ? a[j + H] : a[j];
+                    a[j] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, M);
+                }
+                XReduce<H, M / 2>::run(a, lt);
+            } else {
+                a[0] += __shfl_xor_sync(0xFFFFFFFFu, a[0], M);
+                XReduce<1, M / 2>::run(a, lt);
+            }
+        }
+    }
+};
+
+struct QkInfo { int u, i, valid, mask; };
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kQkThreads, 1)
+qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, DecodeLayout L,
+          int nslots, int group) {
+    using C = QkCfg<T, D, G>;
+    extern __shared__ __align__(128) unsigned char s_raw[];
+    __shared__ int red[40];
+    const int P = kv.P;
+    const uint32_t page_bytes = static_cast<uint32_t>(P * D * sizeof(T));
+    // shared layout: ring [nslots][page] | staging [consumers][G * P] floats |
+    // prefix [U + 1] ints | info [nslots] | full, empty barriers [nslots] each
+    unsigned char* ring = s_raw;
+    float* stage = reinterpret_cast<float*>(s_raw + (size_t)nslots * page_bytes);
+    int* prefix = reinterpret_cast<int*>(stage + kQkConsumers * G * P);
+    QkInfo* info = reinterpret_cast<QkInfo*>(prefix + ((L.U + 1 + 3) & ~3));
+    uint64_t* full = reinterpret_cast<uint64_t*>(info + nslots);
+    uint64_t* empty = full + nslots;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    {
+        // exclusive prefix over units of the union sizes
+        const int U = L.U;
+        const int seg = (U + blockDim.x - 1) / blockDim.x;
+        const int a0 = min(U, tid * seg), a1 = min(U, a0 + seg);
+        int c = 0;
+        for (int a = a0; a < a1; ++a) c += ws.union_count[a];
+        int tot;
+        int run = block_exclusive_scan(c, red, &tot);
+        for (int a = a0; a < a1; ++a) {
+            prefix[a] = run;
+            run += ws.union_count[a];
+        }
+        if (tid == 0) prefix[U] = tot;
     }
     if (tid == 0) {
-        for (int s = 0; s < nstages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < nslots; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
         mbar_fence_init();
     }
-    const int lane = tid & 31, wid = tid >> 5;
-    const int lt = lane % S::LPT;                  // lane within its token group
-    float qr[G][S::CPL][S::EPC];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int cc = 0; cc < S::CPL; ++cc)
-#pragma unroll
-            for (int e = 0; e < S::EPC; ++e)
-                qr[h][cc][e] = qscale *
-                    q[((int64_t)b * Hq + kvh * G + h) * D + (lt + cc * S::LPT) * S::EPC + e];
     __syncthreads();
+    const int total = prefix[L.U];
+    const int f0 = (int)((int64_t)total * blockIdx.x / gridDim.x);
+    const int f1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+    const int nloc = f1 - f0;
+    if (nloc <= 0) return;
 
-    const size_t page_elems = (size_t)P * D;
-    const uint32_t page_bytes = (uint32_t)(page_elems * sizeof(T));
-    const int n_st = (npg + sp - 1) / sp;
-    T* stage0 = reinterpret_cast<T*>(s_raw);
-    const T* kbase = static_cast<const T*>(kv.k);
-    auto issue = [&](int s) {
-        const int slot = s % nstages;
-        const int j0 = s * sp, j1 = min(npg, j0 + sp);
-        mbar_arrive_expect_tx(&bars[slot], page_bytes * (uint32_t)(j1 - j0));
-        for (int j = j0; j < j1; ++j) {
-            const T* src = kbase + ((int64_t)s_blk[j] * kv.hkv + kvh) * page_elems;
-            bulk_g2s(stage0 + (size_t)slot * sp * page_elems + (size_t)(j - j0) * page_elems, src,
-                     page_bytes, &bars[slot]);
+    if (warp == 0) {
+        // ---- producer: page k (0-based within this CTA) goes to slot k % nslots
+        int lo = 0, hi = L.U - 1;       // last unit whose range starts at or before f0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= f0) lo = mid; else hi = mid - 1;
         }
-    };
-    if (tid == 0)
-        for (int s = 0; s < min(nstages, n_st); ++s) issue(s);
+        int cu = lo, ci = f0 - prefix[lo];
+        const T* kbase = static_cast<const T*>(kv.k);
+        for (int g = 0; g < nloc; g += group) {
+            const int k = g + lane;
+            const bool act = lane < group && k < nloc;
+            int uu = cu, ii = ci + lane;
+            if (act)
+                while (ii >= prefix[uu + 1] - prefix[uu]) { ii -= prefix[uu + 1] - prefix[uu]; ++uu; }
+            ci += group;
+            while (cu < L.U && ci >= prefix[cu + 1] - prefix[cu]) { ci -= prefix[cu + 1] - prefix[cu]; ++cu; }
+            if (act) {
+                const int idx = uu * L.Umax + ii;
+                const int page = ws.union_page[idx];
+                const int mask = ws.union_mask[idx];
+                const int b = uu / kv.hkv;
+                const int kvh = uu - b * kv.hkv;
+                const int blk = kv.pt[(int64_t)b * kv.maxp + page];
+                int valid = min(P, kv.sl[b] - page * P);
+                if (blk < 0 || blk >= kv.nb) {
+                    flag_bad_data();
+                    valid = 0;
+                }
+                const int slot = k % nslots;
+                const int use = k / nslots;
+                if (use > 0 && !mbar_wait(&empty[slot], (uint32_t)((use - 1) & 1))) {
+                    flag_bad_data();      // a consumer stalled: hand over an empty page
+                    valid = 0;
+                }
+                info[slot] = QkInfo{uu, ii, valid, mask};
+                if (valid > 0) {
+                    mbar_arrive_expect_tx(&full[slot], page_bytes);
+                    bulk_g2s(ring + (size_t)slot * page_bytes,
+                             kbase + ((int64_t)blk * kv.hkv + kvh) * P * D, page_bytes, &full[slot]);
+                } else {
+                    mbar_arrive(&full[slot]);
+                }
+            }
+            // Lanes move to the next group together.  A lane running ahead
+            // could otherwise wait on a slot's empty barrier two phases early,
+            // and a parity wait would take the still-open phase as complete.
+            __syncwarp();
+        }
+        return;
+    }
 
-    float* zb = ws.z + ((int64_t)b * Hq + kvh * G) * L.zcap;
-    const int stage_tokens = sp * P;
-    for (int s = 0; s < n_st; ++s) {
-        const int slot = s % nstages;
-        const bool ok = mbar_wait(&bars[slot], (uint32_t)((s / nstages) & 1));
-        if (!__syncthreads_and(ok)) {
-            if (tid == 0) flag_bad_data();
-            return;
+    // ---- consumers: warp cw takes pages k = cw (mod consumers); nslots is a
+    // multiple of the consumer count, so every slot has a single owner warp
+    const int cw = warp - 1;
+    const int lt = lane % C::LPT;
+    const int tok = lane / C::LPT;
+    float* st = stage + cw * G * P;
+    float qr[G][C::CPL][C::EPC];
+    float hm[G];
+    int cur_u = -1;
+#define EKV_QK_FLUSH_MAX()                                                                     \
+    do {                                                                                       \
+        const int fb = cur_u / kv.hkv;                                                         \
+        const int fk = cur_u - fb * kv.hkv;                                                    \
+        _Pragma("unroll") for (int h = 0; h < G; ++h) {                                        \
+            const float m = warp_max(hm[h]);                                                   \
+            if (lane == 0 && m > -INFINITY)                                                    \
+                atomicMax(&ws.head_max[fb * Hq + fk * G + h], float_key(m));                   \
+        }                                                                                      \
+    } while (0)
+    for (int k = cw; k < nloc; k += kQkConsumers) {
+        const int slot = k % nslots;
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], (uint32_t)((k / nslots) & 1)));
+        if (!ok) {
+            if (lane == 0) flag_bad_data();
+            break;
         }
-        const T* st = stage0 + (size_t)slot * sp * page_elems;
-        const int pages_here = min(npg, (s + 1) * sp) - s * sp;
-        for (int t0 = 0; t0 < stage_tokens; t0 += S::TPP) {
-            const int ts = t0 + wid * S::TPW + lane / S::LPT;     // token within stage
-            const int jp = ts / P, t = ts - jp * P;
-            const bool live = ts < stage_tokens && jp < pages_here;
+        const QkInfo in = info[slot];
+        if (in.u != cur_u) {
+            if (cur_u >= 0) EKV_QK_FLUSH_MAX();
+            cur_u = in.u;
+            const int b = cur_u / kv.hkv;
+            const int kvh = cur_u - b * kv.hkv;
+            const float* qb = q + ((int64_t)b * Hq + kvh * G) * D;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                hm[h] = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < C::CPL; ++cc)
+#pragma unroll
+                    for (int e = 0; e < C::EPC; ++e)
+                        qr[h][cc][e] = qscale * qb[h * D + (lt + cc * C::LPT) * C::EPC + e];
+            }
+        }
+        const T* pg = reinterpret_cast<const T*>(ring + (size_t)slot * page_bytes);
+        for (int t0 = 0; t0 < P; t0 += C::TPW) {
+            const int t = t0 + tok;
+            const T* row = pg + (size_t)t * D;
             float acc[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) acc[h] = 0.f;
-            if (live) {
-                const T* row = st + (size_t)ts * D;
 #pragma unroll
-                for (int cc = 0; cc < S::CPL; ++cc) {
-                    const uint4 raw =
-                        *reinterpret_cast<const uint4*>(row + (lt + cc * S::LPT) * S::EPC);
-                    float x[S::EPC];
-                    Elem<T>::widen(raw, x);
+            for (int cc = 0; cc < C::CPL; ++cc) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(row + (lt + cc * C::LPT) * C::EPC);
+                float x[C::EPC];
+                Elem<T>::widen(raw, x);
 #pragma unroll
-                    for (int h = 0; h < G; ++h)
+                for (int h = 0; h < G; ++h)
 #pragma unroll
-                        for (int e = 0; e < S::EPC; ++e) acc[h] = fmaf(qr[h][cc][e], x[e], acc[h]);
-                }
+                    for (int e = 0; e < C::EPC; ++e) acc[h] = fmaf(qr[h][cc][e], x[e], acc[h]);
             }
+            XReduce<G, C::LPT / 2>::run(acc, lt);
+            if (lt % C::DUP == 0) st[(lt / C::DUP) * P + t] = acc[0];
+        }
+        __syncwarp();
+        for (int e = lane * 4; e < G * P; e += 128) {
+            const int h = e / P, t = e - h * P;
+            float4 v = *reinterpret_cast<const float4*>(st + e);
+            const bool hin = (in.mask >> h) & 1;
+            v.x = (hin && t + 0 < in.valid) ? v.x : -INFINITY;
+            v.y = (hin && t + 1 < in.valid) ? v.y : -INFINITY;
+            v.z = (hin && t + 2 < in.valid) ? v.z : -INFINITY;
+            v.w = (hin && t + 3 < in.valid) ? v.w : -INFINITY;
+            *reinterpret_cast<float4*>(ws.z + (((int64_t)in.u * G + h) * L.Umax + in.i) * P + t) = v;
+            const float m4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
 #pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = group_sum<S::LPT>(acc[h]);
-            if (live && lt < G) {
-                const int pg = s * sp + jp;
-                float mine = 0.f;
-#pragma unroll
-                for (int h = 0; h < G; ++h) if (lt == h) mine = acc[h];
-                if ((s_mask[pg] >> lt) & 1) {
-                    const int rank = s_rank[pg][lt];
-                    zb[(int64_t)lt * L.zcap + (int64_t)rank * P + t] = t < s_valid[pg] ? mine : -INFINITY;
-                }
+            for (int hh = 0; hh < G; ++hh)
+                if (hh == h) hm[hh] = fmaxf(hm[hh], m4);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (cur_u >= 0) EKV_QK_FLUSH_MAX();
+#undef EKV_QK_FLUSH_MAX
+}
+
+// ---------------------------------------------------------------------------
+// qk for bf16 K on the tensor cores (mma.sync m16n8k16, fp32 accumulate).
+//
+// A = q of the group as 3G bf16 rows: each fp32 q (times (alpha-1) s) is split
+// exactly into hi + mid + lo bf16 terms, so that the bf16 x bf16 products are
+// exact and the three rows of a head sum to the fp32 score.  B = the K page:
+// n = tokens, k = head dimensions.  The contraction order over k is free, so
+// the k positions are permuted (identically in A and B) such that one 16-byte
+// read of 8 consecutive dimensions of one token fills the B fragments of two
+// k-steps: lane (g, t) reads token g, dimensions [32 dg + 8 t, +8).
+//
+// Every warp streams its own contiguous range of the flattened union lists
+// through a private ring of NS page stages in shared memory: one bulk copy per
+// page on the warp's own mbarriers (no handshake between warps), the copy of
+// page k + NS - 1 issued as soon as page k - 1 has been consumed.
+// ---------------------------------------------------------------------------
+constexpr int kQmWarps = 4;                  // warps per CTA
+constexpr int kQmCtasPerSm = 2;
+constexpr int kQmStageBytes = 24 * 1024;     // ring bytes per warp
+
+template <int D, int G>
+struct QmCfg {
+    static constexpr int NR = 3 * G;              // (split, head) rows of A
+    static constexpr int MT = (NR + 15) / 16;     // m-tiles
+    static constexpr int KS = D / 16;             // k-steps
+};
+
+__device__ __forceinline__ uint32_t bf16_rn_bits(float x) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+}
+
+// Term s (0 hi, 1 mid, 2 lo) of the exact three-way bf16 split of x.
+__device__ __forceinline__ uint32_t split_term(float x, int s) {
+    const uint32_t hi = bf16_rn_bits(x);
+    const float r1 = x - __uint_as_float(hi << 16);
+    const uint32_t mid = bf16_rn_bits(r1);
+    const float r2 = r1 - __uint_as_float(mid << 16);
+    const uint32_t lo = bf16_rn_bits(r2);
+    return s == 0 ? hi : (s == 1 ? mid : lo);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+struct PgDesc { int blk, u, i, valid, mask; };
+
+__device__ __forceinline__ PgDesc resolve_page(int f, int f1, const int* prefix, const KV& kv,
+                                               const WS& ws, const DecodeLayout& L) {
+    PgDesc d{-1, 0, 0, 0, 0};
+    if (f >= f1) return d;
+    int lo = 0, hi = L.U - 1;    // last unit whose range starts at or before f
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= f) lo = mid; else hi = mid - 1;
+    }
+    d.u = lo;
+    d.i = f - prefix[lo];
+    const int idx = lo * L.Umax + d.i;
+    const int page = __ldcg(ws.union_page + idx);
+    d.mask = __ldcg(ws.union_mask + idx);
+    const int b = lo / kv.hkv;
+    int blk = kv.pt[(int64_t)b * kv.maxp + page];
+    d.valid = min(kv.P, kv.sl[b] - page * kv.P);
+    if (blk < 0 || blk >= kv.nb) {
+        flag_bad_data();
+        blk = -1;
+        d.valid = 0;
+    }
+    d.blk = blk;
+    return d;
+}
+
+__device__ __forceinline__ PgDesc shfl_desc(const PgDesc& d, int src) {
+    return PgDesc{__shfl_sync(0xFFFFFFFFu, d.blk, src), __shfl_sync(0xFFFFFFFFu, d.u, src),
+                  __shfl_sync(0xFFFFFFFFu, d.i, src), __shfl_sync(0xFFFFFFFFu, d.valid, src),
+                  __shfl_sync(0xFFFFFFFFu, d.mask, src)};
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kQmWarps * 32, kQmCtasPerSm)
+qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, DecodeLayout L,
+              int ns) {
+    using C = QmCfg<D, G>;
+    extern __shared__ __align__(128) unsigned char s_qm[];
+    __shared__ int red[40];
+    __shared__ __align__(8) uint64_t s_bar[kQmWarps][8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int P = kv.P;
+    const uint32_t page_bytes = static_cast<uint32_t>(P * D * 2);
+    // shared layout: per-warp rings [warps][ns][page] | unit prefix [U + 1]
+    unsigned char* ring = s_qm + (size_t)warp * ns * page_bytes;
+    int* s_prefix = reinterpret_cast<int*>(s_qm + (size_t)kQmWarps * ns * page_bytes);
+    uint64_t* bar = s_bar[warp];
+    {
+        const int U = L.U;
+        const int seg = (U + blockDim.x - 1) / blockDim.x;
+        const int a0 = min(U, tid * seg), a1 = min(U, a0 + seg);
+        int c = 0;
+        for (int a = a0; a < a1; ++a) c += __ldcg(ws.union_count + a);
+        int tot;
+        int run = block_exclusive_scan(c, red, &tot);
+        for (int a = a0; a < a1; ++a) {
+            s_prefix[a] = run;
+            run += __ldcg(ws.union_count + a);
+        }
+        if (tid == 0) s_prefix[U] = tot;
+    }
+    if (lane == 0) {
+        for (int st = 0; st < ns; ++st) mbar_init(&bar[st], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int total = s_prefix[L.U];
+    const int64_t nwg = (int64_t)gridDim.x * kQmWarps;
+    const int wg = blockIdx.x * kQmWarps + warp;
+    const int f0 = (int)((int64_t)total * wg / nwg);
+    const int f1 = (int)((int64_t)total * (wg + 1) / nwg);
+    const int npg = f1 - f0;
+    if (npg <= 0) return;
+    const unsigned char* kbase = static_cast<const unsigned char*>(kv.k);
+
+    PgDesc cur = resolve_page(f0 + lane, f1, s_prefix, kv, ws, L);
+    PgDesc nxt = resolve_page(f0 + 32 + lane, f1, s_prefix, kv, ws, L);
+    int cur_base = 0;
+    // Issues page k into stage k % ns; returns its descriptor.
+    auto issue = [&](int k) -> PgDesc {
+        PgDesc dsc{-1, 0, 0, 0, 0};
+        if (k >= npg) return dsc;
+        if (k >= cur_base + 32) {
+            cur = nxt;
+            cur_base += 32;
+            nxt = resolve_page(f0 + cur_base + 32 + lane, f1, s_prefix, kv, ws, L);
+        }
+        dsc = shfl_desc(cur, k - cur_base);
+        if (lane == 0) {
+            const int st = k % ns;
+            if (dsc.blk >= 0) {
+                mbar_arrive_expect_tx(&bar[st], page_bytes);
+                bulk_g2s(ring + (size_t)st * page_bytes,
+                         kbase + (((int64_t)dsc.blk * kv.hkv + dsc.u % kv.hkv) * P * D) * 2,
+                         page_bytes, &bar[st]);
+            } else {
+                mbar_arrive(&bar[st]);
             }
         }
-        __syncthreads();
-        if (tid == 0 && s + nstages < n_st) issue(s + nstages);
+        return dsc;
+    };
+
+    uint32_t a[C::MT][C::KS][4];
+    float hm = -INFINITY;                 // running max of head g (lanes g < G)
+    int cur_u = -1;
+    PgDesc dq[8];            // descriptor of the page held by each stage (ns <= 8)
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+        if (x < ns - 1) dq[x] = issue(x);
+    bool failed = false;
+    for (int k = 0; k < npg; ++k) {
+        const int st = k % ns;
+        // stage (k - 1) % ns was consumed in the previous iteration
+        {
+            const PgDesc nd = issue(k + ns - 1);
+            const int nst = (k + ns - 1) % ns;
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                if (x == nst) dq[x] = nd;
+        }
+        PgDesc d{};
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+            if (x == st) d = dq[x];
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[st], (uint32_t)((k / ns) & 1)))) {
+            failed = true;
+            break;
+        }
+        if (d.u != cur_u) {
+            if (cur_u >= 0) {
+                float m = fmaxf(hm, __shfl_xor_sync(0xFFFFFFFFu, hm, 1));
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                const int fb = cur_u / kv.hkv, fk = cur_u - fb * kv.hkv;
+                if (t == 0 && g < G && m > -INFINITY)
+                    atomicMax(&ws.head_max[fb * Hq + fk * G + g], float_key(m));
+            }
+            cur_u = d.u;
+            hm = -INFINITY;
+            const int b = cur_u / kv.hkv, kvh = cur_u - b * kv.hkv;
+            const float* qb = q + ((int64_t)b * Hq + kvh * G) * D;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+                for (int kk = 0; kk < C::KS; ++kk)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int row = mt * 16 + g + ((r & 1) ? 8 : 0);
+                        const int dim = 32 * (kk >> 1) + 8 * t + 4 * (kk & 1) + ((r & 2) ? 2 : 0);
+                        uint32_t v = 0;
+                        if (row < C::NR) {
+                            const int sp = row / G, hh2 = row - sp * G;
+                            const float x0 = qscale * __ldg(qb + hh2 * D + dim);
+                            const float x1 = qscale * __ldg(qb + hh2 * D + dim + 1);
+                            v = split_term(x0, sp) | (split_term(x1, sp) << 16);
+                        }
+                        a[mt][kk][r] = v;
+                    }
+        }
+        const unsigned char* pg = ring + (size_t)st * page_bytes;
+        for (int nt = 0; nt < P / 8; ++nt) {
+            float c[C::MT][4];
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) c[mt][e] = 0.f;
+            const unsigned char* row = pg + (size_t)(nt * 8 + g) * D * 2 + 16 * t;
+#pragma unroll
+            for (int dg = 0; dg < D / 32; ++dg) {
+                const uint4 v = *reinterpret_cast<const uint4*>(row + 64 * dg);
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    mma_bf16(c[mt], a[mt][2 * dg], v.x, v.y);
+                    mma_bf16(c[mt], a[mt][2 * dg + 1], v.z, v.w);
+                }
+            }
+            // z(head g, token) = sum over the three split rows s G + g
+            float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+            for (int sp = 0; sp < 3; ++sp) {
+                const int r0 = sp * G;                 // row of head 0 in this split
+                const int mt = r0 / 16, hf = (r0 % 16) / 8;
+                float v0 = c[mt][2 * hf], v1 = c[mt][2 * hf + 1];
+                if ((r0 % 8) != 0) {
+                    const int src = (((r0 + g) % 8) << 2) | t;
+                    v0 = __shfl_sync(0xFFFFFFFFu, v0, src);
+                    v1 = __shfl_sync(0xFFFFFFFFu, v1, src);
+                }
+                z0 += v0;
+                z1 += v1;
+            }
+            if (g < G) {
+                const int tok = nt * 8 + 2 * t;
+                const bool hin = (d.mask >> g) & 1;
+                z0 = (hin && tok < d.valid) ? z0 : -INFINITY;
+                z1 = (hin && tok + 1 < d.valid) ? z1 : -INFINITY;
+                *reinterpret_cast<float2*>(ws.z + (((int64_t)d.u * G + g) * L.Umax + d.i) * P + tok) =
+                    make_float2(z0, z1);
+                hm = fmaxf(hm, fmaxf(z0, z1));
+            }
+        }
+        __syncwarp();        // every lane is done with stage st before it is refilled
+    }
+    if (failed) {
+        if (lane == 0) flag_bad_data();
+        return;
+    }
+    {
+        float m = fmaxf(hm, __shfl_xor_sync(0xFFFFFFFFu, hm, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        const int fb = cur_u / kv.hkv, fk = cur_u - fb * kv.hkv;
+        if (cur_u >= 0 && t == 0 && g < G && m > -INFINITY)
+            atomicMax(&ws.head_max[fb * Hq + fk * G + g], float_key(m));
     }
 }
 
@@ -326,21 +684,25 @@ __device__ __forceinline__ float pow_e(float a, int E, float ex) {
 
 template <int E>   // 2: alpha = 1.5, 1: alpha = 2, 0: any other alpha
 __global__ void __launch_bounds__(kTauThreads)
-tau_kernel(float alpha, int P, WS ws, DecodeLayout L, float* __restrict__ tau_out,
-           int32_t* __restrict__ support_out) {
-    extern __shared__ __align__(16) float s_buf[];
+tau_kernel(int Hq, int P, float alpha, int cand_cap, WS ws, DecodeLayout L,
+           float* __restrict__ tau_out, int32_t* __restrict__ support_out) {
+    extern __shared__ __align__(16) float s_x[];     // [cand_cap] values, then positions, bitmap
+    int* s_pos = reinterpret_cast<int*>(s_x + cand_cap);
+    uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_pos + cand_cap);
     __shared__ float fred[40];
     __shared__ float2 f2red[32];
     __shared__ int ired[40];
-    __shared__ int s_m;
-    __shared__ float s_pref[2];
-    __shared__ int s_kstar;
 
     const int bh = blockIdx.x;
-    const int n = ws.head_count[bh] * P;
-    const float* z = ws.z + (int64_t)bh * L.zcap;
+    const int G = L.G;
+    const int b = bh / Hq;
+    const int h = bh - b * Hq;
+    const int u = b * (Hq / G) + h / G;
+    const int hg = h % G;
     const int tid = threadIdx.x;
-    if (n <= 0) {
+    const uint32_t key = ws.head_max[bh];
+    const int n = ws.union_count[u] * P;
+    if (key == 0u || n == 0) {
         if (tid == 0) {
             ws.tau[bh] = INFINITY;
             if (tau_out) tau_out[bh] = INFINITY;
@@ -348,27 +710,54 @@ tau_kernel(float alpha, int P, WS ws, DecodeLayout L, float* __restrict__ tau_ou
         }
         return;
     }
-    float mx = -INFINITY;
-    for (int i = tid; i < n; i += blockDim.x) mx = fmaxf(mx, z[i]);
-    mx = block_max(mx, fred);
-    if (tid == 0) s_m = 0;
-    __syncthreads();
-    // candidates: x = z' - max > -1 (anything lower has zero weight)
-    for (int i = tid; i < n; i += blockDim.x) {
-        const float x = z[i] - mx;
-        if (x > -1.f) s_buf[atomicAdd(&s_m, 1)] = x;
+    const float mx = key_float(key);
+    const float* z = ws.z + ((int64_t)u * G + hg) * L.Umax * P;
+    for (int i = tid; i < L.nbw; i += blockDim.x) s_bits[i] = 0u;
+
+    // candidates x = z' - max > -1 (all others have zero weight).  Each tile
+    // is read with coalesced 16-byte loads, all in flight at once, and
+    // compacted in a fixed thread order (deterministic sums below).
+    constexpr int kVec = 8;                                // float4 per thread per tile
+    constexpr int kTile = kTauThreads * kVec * 4;
+    int m = 0;
+    for (int t0 = 0; t0 < n; t0 += kTile) {
+        float v[kVec * 4];
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const int i = t0 + (j * kTauThreads + tid) * 4;   // n is a multiple of 4
+            const float4 f = i < n ? __ldcg(reinterpret_cast<const float4*>(z + i))
+                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            v[4 * j] = f.x - mx; v[4 * j + 1] = f.y - mx; v[4 * j + 2] = f.z - mx; v[4 * j + 3] = f.w - mx;
+        }
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < kVec * 4; ++j) c += v[j] > -1.f;
+        int tot;
+        int pos = m + block_exclusive_scan(c, ired, &tot);
+#pragma unroll
+        for (int j = 0; j < kVec * 4; ++j) {
+            if (v[j] > -1.f) {
+                if (pos < cand_cap) {
+                    s_x[pos] = v[j];
+                    s_pos[pos] = t0 + ((j >> 2) * kTauThreads + tid) * 4 + (j & 3);
+                }
+                ++pos;
+            }
+        }
+        m += tot;
     }
+    m = min(m, cand_cap);
     __syncthreads();
-    const int m = s_m;
-    const float ex = 1.f / (alpha - 1.f);
+
     float t;
     if (E == 0) {
+        const float ex = 1.f / (alpha - 1.f);
         float lo = -1.f, hi = -powf(static_cast<float>(m), 1.f - alpha);
         for (int it = 0; it < 48; ++it) {
             const float mid = 0.5f * (lo + hi);
             float f = 0.f;
             for (int i = tid; i < m; i += blockDim.x) {
-                const float a = s_buf[i] - mid;
+                const float a = s_x[i] - mid;
                 if (a > 0.f) f += powf(a, ex);
             }
             f = block_sum(f, fred) - 1.f;
@@ -376,96 +765,39 @@ tau_kernel(float alpha, int P, WS ws, DecodeLayout L, float* __restrict__ tau_ou
         }
         t = 0.5f * (lo + hi);
     } else {
-        int M = 1;
-        while (M < m) M <<= 1;
-        for (int i = m + tid; i < M; i += blockDim.x) s_buf[i] = -INFINITY;
-        __syncthreads();
-        // bitonic sort, descending
-        for (int k = 2; k <= M; k <<= 1) {
-            for (int j = k >> 1; j > 0; j >>= 1) {
-                for (int i = tid; i < M; i += blockDim.x) {
-                    const int ij = i ^ j;
-                    if (ij > i) {
-                        const float a = s_buf[i], c = s_buf[ij];
-                        const bool desc = (i & k) == 0;
-                        if (desc ? (a < c) : (a > c)) { s_buf[i] = c; s_buf[ij] = a; }
-                    }
-                }
-                __syncthreads();
-            }
-        }
-        // prefix sums over contiguous segments of the sorted candidates
-        const int seg = (m + blockDim.x - 1) / blockDim.x;
-        const int k0 = min(m, tid * seg), k1 = min(m, k0 + seg);
-        float a1 = 0.f, a2 = 0.f;
-        for (int i = k0; i < k1; ++i) { a1 += s_buf[i]; a2 = fmaf(s_buf[i], s_buf[i], a2); }
-        const float inc1 = block_inclusive_scan_f(a1, fred);
-        const float inc2 = block_inclusive_scan_f(a2, fred);
-        float S1 = inc1 - a1, S2 = inc2 - a2;
-        int best = 1;
-        for (int i = k0; i < k1; ++i) {
-            const float x = s_buf[i];
-            S1 += x;
-            S2 = fmaf(x, x, S2);
-            const int kk = i + 1;
-            bool valid;
-            if (E == 1) {
-                valid = x > (S1 - 1.f) / kk;
-            } else {
-                const float Mk = S1 / kk;
-                const float ss = fmaxf(S2 - S1 * Mk, 0.f);
-                valid = ss <= 1.f && (Mk - sqrtf((1.f - ss) / kk)) <= x;
-            }
-            if (valid) best = kk;
-        }
-        // k* = largest valid prefix length
-        int kstar = best;
-        {
-            int v = kstar;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-            __syncthreads();
-            if ((tid & 31) == 0) ired[tid >> 5] = v;
-            __syncthreads();
-            v = (tid & 31) < (int)(blockDim.x >> 5) ? ired[tid & 31] : 0;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-            kstar = v;
-        }
-        if (kstar - 1 >= k0 && kstar - 1 < k1) {
-            // the owner of position k* recomputes its prefix sums
-            float P1 = inc1 - a1, P2 = inc2 - a2;
-            for (int i = k0; i < kstar; ++i) { P1 += s_buf[i]; P2 = fmaf(s_buf[i], s_buf[i], P2); }
-            s_pref[0] = P1;
-            s_pref[1] = P2;
-            s_kstar = kstar;
-        }
-        __syncthreads();
-        const float P1 = s_pref[0], P2 = s_pref[1];
-        if (E == 1) {
-            t = (P1 - 1.f) / kstar;
-        } else {
-            const float Mk = P1 / kstar;
-            const float ss = fmaxf(P2 - P1 * Mk, 0.f);
-            t = Mk - sqrtf(fmaxf(1.f - ss, 0.f) / kstar);
-        }
-        // Newton polish on f(t) = sum (x - t)_+^e - 1 (exact piecewise form)
-        for (int it = 0; it < 3; ++it) {
+        // Newton on f(t) = sum (x - t)_+^e - 1 from t = -1 (f >= 0 there: the
+        // maximum alone contributes 1); f is convex and decreasing, so the
+        // iterates increase monotonically to the root.
+        t = -1.f;
+        for (int it = 0; it < 64; ++it) {
             float2 acc = make_float2(0.f, 0.f);
             for (int i = tid; i < m; i += blockDim.x) {
-                const float a = s_buf[i] - t;
+                const float a = s_x[i] - t;
                 if (a > 0.f) {
-                    if (E == 2) { acc.x = fmaf(a, a, acc.x); acc.y += 2.f * a; }
+                    if (E == 2) { acc.x = fmaf(a, a, acc.x); acc.y += a; }
                     else { acc.x += a; acc.y += 1.f; }
                 }
             }
             acc = block_sum2(acc, f2red);
-            if (acc.y > 0.f) t += (acc.x - 1.f) / acc.y;
+            const float dv = E == 2 ? 2.f * acc.y : acc.y;
+            if (!(dv > 0.f)) break;
+            const float step = (acc.x - 1.f) / dv;
+            t += step;
+            if (!(step > 1e-7f)) break;     // at the root to fp32 resolution
         }
     }
+    // support and the pages holding it
     int sup = 0;
-    for (int i = tid; i < m; i += blockDim.x) sup += s_buf[i] > t;
+    for (int i = tid; i < m; i += blockDim.x) {
+        if (s_x[i] > t) {
+            ++sup;
+            const int page = s_pos[i] / P;
+            atomicOr(&s_bits[page >> 5], 1u << (page & 31));
+        }
+    }
     sup = block_sum_i(sup, ired);
+    for (int i = tid; i < L.nbw; i += blockDim.x)
+        if (s_bits[i]) atomicOr(&ws.supp[(int64_t)u * L.nbw + i], s_bits[i]);
     if (tid == 0) {
         const float tau = t + mx;
         ws.tau[bh] = tau;
@@ -475,186 +807,220 @@ tau_kernel(float alpha, int P, WS ws, DecodeLayout L, float* __restrict__ tau_ou
 }
 
 // ---------------------------------------------------------------------------
-// pv: weights, value accumulation over the support pages, merge
+// pv: weights and value accumulation over the support pages, merge
 // ---------------------------------------------------------------------------
+// Persistent: a work item is (unit, chunk of up to chv support pages); a unit
+// with no support page gets one item that writes zeros.  CTA i takes items
+// i, i + gridDim.x, ...
 template <typename T, int D, int G, int E>
 __global__ void __launch_bounds__(kPvThreads)
-pv_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __restrict__ out,
-          int nstages) {
+pv_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __restrict__ out, int chv) {
     constexpr int EPC = Elem<T>::kPer16;
-    constexpr int LPR = D / EPC;          // lanes per value row
-    constexpr int RPW = 32 / LPR;         // rows per warp pass
-    constexpr int NW = kPvThreads / 32;
-    constexpr int RPP = NW * RPW;         // rows per CTA pass
+    constexpr int LPR = D / EPC;              // lanes per value row
+    constexpr int RG = kPvThreads / LPR;      // row groups
+    constexpr int NWP = kPvThreads / 32;
     extern __shared__ __align__(128) unsigned char s_raw[];
-    __shared__ __align__(8) uint64_t bars[8];
-    __shared__ int s_blk[kChunkPages], s_page_ok[kChunkPages], s_act[kChunkPages];
-    __shared__ float s_tau[G];
-    __shared__ float s_psum[G];
-    __shared__ int s_nact, s_last;
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_act[kPvMaxChunk], s_blk[kPvMaxChunk];
+    __shared__ int red[40];
+    __shared__ float s_tau[G], s_psum[G];
+    __shared__ float s_wps[NWP][G];
+    __shared__ int s_last;
 
-    const int u = blockIdx.y;
-    const int c = blockIdx.x;
-    const int b = u / kv.hkv;
-    const int kvh = u % kv.hkv;
     const int P = kv.P;
-    const int tid = threadIdx.x;
-    const int ucnt = ws.union_count[u];
-    const int nchunks = (ucnt + L.CH - 1) / L.CH;
-    float* outb = out + ((int64_t)b * Hq + kvh * G) * D;
-    if (ucnt == 0) {
-        if (c == 0)
-            for (int i = tid; i < G * D; i += blockDim.x) outb[i] = 0.f;
-        return;
-    }
-    if (c >= nchunks) return;
-    const int i0 = c * L.CH;
-    const int npg = min(ucnt, i0 + L.CH) - i0;
-    const int len = kv.sl[b];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const size_t page_elems = (size_t)P * D;
+    const uint32_t page_bytes = (uint32_t)(page_elems * sizeof(T));
+    const size_t vbytes = (size_t)chv * page_bytes, rbytes = (size_t)RG * G * D * sizeof(float);
+    const size_t stage_bytes = vbytes > rbytes ? vbytes : rbytes;
+    // shared layout: V pages (later the reduction buffer) | weights [chv][P][G]
+    // | support pages per unit [U] | first work item per unit [U + 1]
+    T* stage = reinterpret_cast<T*>(s_raw);
+    float* s_red = reinterpret_cast<float*>(s_raw);
+    float* s_w = reinterpret_cast<float*>(s_raw + stage_bytes);
+    int* s_nact = reinterpret_cast<int*>(s_w + (size_t)chv * P * G);
+    int* s_start = s_nact + L.U;
 
-    // shared layout: weights [CH][P][G], reduction [RPP][G][D], V stages
-    float* s_w = reinterpret_cast<float*>(s_raw);
-    float* s_red = s_w + (size_t)kChunkPages * P * G;
-    T* stage0 = reinterpret_cast<T*>(s_red + (size_t)RPP * G * D);
-
-    if (tid < G) {
-        s_tau[tid] = ws.tau[b * Hq + kvh * G + tid];
-        s_psum[tid] = 0.f;
-    }
-    if (tid < kChunkPages) s_page_ok[tid] = 0;
-    if (tid < npg) {
-        const int idx = u * L.Umax + i0 + tid;
-        const int page = ws.union_page[idx];
-        int blk = kv.pt[(int64_t)b * kv.maxp + page];
-        if (blk < 0 || blk >= kv.nb) blk = -1;
-        s_blk[tid] = blk;
-    }
+    for (int i = tid; i < L.U; i += blockDim.x) s_nact[i] = 0;
     if (tid == 0) {
-        for (int s = 0; s < nstages; ++s) mbar_init(&bars[s], 1);
+        mbar_init(&bar, 1);
         mbar_fence_init();
     }
     __syncthreads();
-
-    const float ex = 1.f / (alpha - 1.f);
-    const float* zb = ws.z + ((int64_t)b * Hq + kvh * G) * L.zcap;
-    float ps[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) ps[h] = 0.f;
-    for (int i = tid; i < npg * P; i += blockDim.x) {
-        const int pg = i / P, t = i - pg * P;
-        const int idx = u * L.Umax + i0 + pg;
-        const int mask = ws.union_mask[idx];
-        const int page = ws.union_page[idx];
-        const bool tok_ok = s_blk[pg] >= 0 && t < min(P, len - page * P);
-        bool any = false;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float w = 0.f;
-            if (tok_ok && ((mask >> h) & 1)) {
-                const int rank = ws.union_rank[(int64_t)idx * G + h];
-                const float a = zb[(int64_t)h * L.zcap + (int64_t)rank * P + t] - s_tau[h];
-                if (a > 0.f) w = pow_e(a, E, ex);
-            }
-            s_w[((size_t)pg * P + t) * G + h] = w;
-            ps[h] += w;
-            any |= w > 0.f;
+    for (int i = tid; i < L.U * L.nbw; i += blockDim.x) {
+        const int c = __popc(ws.supp[i]);
+        if (c) atomicAdd(&s_nact[i / L.nbw], c);
+    }
+    __syncthreads();
+    {
+        const int seg = (L.U + blockDim.x - 1) / blockDim.x;
+        const int a0 = min(L.U, tid * seg), a1 = min(L.U, a0 + seg);
+        int c = 0;
+        for (int a = a0; a < a1; ++a) c += max(1, (s_nact[a] + chv - 1) / chv);
+        int tot;
+        int run = block_exclusive_scan(c, red, &tot);
+        for (int a = a0; a < a1; ++a) {
+            s_start[a] = run;
+            run += max(1, (s_nact[a] + chv - 1) / chv);
         }
-        if (any) s_page_ok[pg] = 1;
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const float v = warp_sum(ps[h]);
-        if ((tid & 31) == 0) atomicAdd(&s_psum[h], v);
+        if (tid == 0) s_start[L.U] = tot;
     }
     __syncthreads();
-    if (tid == 0) {
-        int n = 0;
-        for (int j = 0; j < npg; ++j)
-            if (s_page_ok[j]) s_act[n++] = j;
-        s_nact = n;
-        if (n) atomicAdd(&ws.vpages[u], n);
-    }
-    __syncthreads();
-    const int nact = s_nact;
-
-    const size_t page_elems = (size_t)P * D;
-    const uint32_t page_bytes = (uint32_t)(page_elems * sizeof(T));
+    const int items = s_start[L.U];
+    const float ex = 1.f / (alpha - 1.f);
     const T* vbase = static_cast<const T*>(kv.v);
-    auto issue = [&](int s) {
-        const int slot = s % nstages;
-        mbar_arrive_expect_tx(&bars[slot], page_bytes);
-        const T* src = vbase + ((int64_t)s_blk[s_act[s]] * kv.hkv + kvh) * page_elems;
-        bulk_g2s(stage0 + (size_t)slot * page_elems, src, page_bytes, &bars[slot]);
-    };
-    if (tid == 0)
-        for (int s = 0; s < min(nstages, nact); ++s) issue(s);
+    uint32_t phase = 0;
 
-    const int lane = tid & 31, wid = tid >> 5;
-    const int lr = lane % LPR;
-    const int rg = wid * RPW + lane / LPR;
-    float acc[G][EPC];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) acc[h][e] = 0.f;
-    bool failed = false;
-    for (int s = 0; s < nact; ++s) {
-        const int slot = s % nstages;
-        const bool ok = mbar_wait(&bars[slot], (uint32_t)((s / nstages) & 1));
-        if (!__syncthreads_and(ok)) { failed = true; break; }
-        const T* st = stage0 + (size_t)slot * page_elems;
-        const float* wp = s_w + (size_t)s_act[s] * P * G;
-        for (int t = rg; t < P; t += RPP) {
-            float x[EPC];
-            Elem<T>::widen(*reinterpret_cast<const uint4*>(st + (size_t)t * D + lr * EPC), x);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float w = wp[t * G + h];
-#pragma unroll
-                for (int e = 0; e < EPC; ++e) acc[h][e] = fmaf(w, x[e], acc[h][e]);
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        int lo = 0, hi = L.U - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_start[mid] <= item) lo = mid; else hi = mid - 1;
+        }
+        const int u = lo;
+        const int c = item - s_start[u];
+        const int nact = s_nact[u];
+        const int b = u / kv.hkv;
+        const int kvh = u - b * kv.hkv;
+        float* outb = out + ((int64_t)b * Hq + kvh * G) * D;
+        if (nact == 0) {            // uniform across the CTA
+            for (int i = tid; i < G * D; i += blockDim.x) outb[i] = 0.f;
+            if (tid == 0) ws.vpages[u] = 0;
+            continue;
+        }
+        const int nchunks = (nact + chv - 1) / chv;
+        const int a0 = c * chv;
+        const int npg = min(nact, a0 + chv) - a0;
+        {
+            // this chunk's support pages, in union order (nbw <= kPvThreads)
+            const uint32_t word = tid < L.nbw ? ws.supp[(int64_t)u * L.nbw + tid] : 0u;
+            int all;
+            int r = block_exclusive_scan(__popc(word), red, &all);
+            uint32_t w = word;
+            while (w && r < a0 + chv) {
+                const int bit = __ffs(w) - 1;
+                w &= w - 1;
+                if (r >= a0) s_act[r - a0] = tid * 32 + bit;
+                ++r;
             }
+        }
+        if (tid < G) s_tau[tid] = ws.tau[b * Hq + kvh * G + tid];
+        if (tid == 0 && c == 0) ws.vpages[u] = nact;
+        __syncthreads();
+        if (tid < npg) {
+            const int page = ws.union_page[(int64_t)u * L.Umax + s_act[tid]];
+            const int blk = kv.pt[(int64_t)b * kv.maxp + page];
+            s_blk[tid] = (blk < 0 || blk >= kv.nb) ? -1 : blk;
         }
         __syncthreads();
-        if (tid == 0 && s + nstages < nact) issue(s + nstages);
-    }
-    if (failed) {
-        if (tid == 0) flag_bad_data();
-        return;
-    }
-    // reduce over the RPP row groups
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) s_red[((size_t)rg * G + h) * D + lr * EPC + e] = acc[h][e];
-    __syncthreads();
-    float* part = ws.partial + ((int64_t)u * L.Smax + c) * G * (D + 1);
-    for (int i = tid; i < G * D; i += blockDim.x) {
-        float sacc = 0.f;
-        for (int g = 0; g < RPP; ++g) sacc += s_red[(size_t)g * G * D + i];
-        part[i] = sacc;
-    }
-    if (tid < G) part[G * D + tid] = s_psum[tid];
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int ticket = atomicAdd(&ws.counter[u], 1);
-        s_last = ticket == nchunks - 1;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const float* part0 = ws.partial + (int64_t)u * L.Smax * G * (D + 1);
-    for (int i = tid; i < G * D; i += blockDim.x) {
-        const int h = i / D;
-        float so = 0.f, sp = 0.f;
-        for (int cc = 0; cc < nchunks; ++cc) {
-            const float* pc = part0 + (int64_t)cc * G * (D + 1);
-            so += __ldcg(pc + i);
-            sp += __ldcg(pc + G * D + h);
+        if (tid == 0) {
+            uint32_t bytes = 0;
+            for (int j = 0; j < npg; ++j) bytes += s_blk[j] >= 0 ? page_bytes : 0u;
+            mbar_arrive_expect_tx(&bar, bytes);
+            for (int j = 0; j < npg; ++j)
+                if (s_blk[j] >= 0)
+                    bulk_g2s(stage + (size_t)j * page_elems,
+                             vbase + ((int64_t)s_blk[j] * kv.hkv + kvh) * page_elems, page_bytes, &bar);
         }
-        outb[i] = sp > 0.f ? so / sp : 0.f;
+
+        // weights, while the copies are in flight
+        float ps[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) ps[h] = 0.f;
+        for (int idx = tid; idx < npg * P; idx += blockDim.x) {
+            const int j = idx / P, t = idx - j * P;
+            const int i = s_act[j];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float a = __ldcg(ws.z + (((int64_t)u * G + h) * L.Umax + i) * P + t) - s_tau[h];
+                const float w = a > 0.f ? pow_e(a, E, ex) : 0.f;
+                s_w[idx * G + h] = w;
+                ps[h] += w;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float v = warp_sum(ps[h]);
+            if (lane == 0) s_wps[wid][h] = v;
+        }
+        const bool ok = __syncthreads_and(mbar_wait(&bar, phase));
+        phase ^= 1u;
+        if (!ok) {
+            if (tid == 0) flag_bad_data();
+            return;
+        }
+        if (tid < G) {
+            float sum = 0.f;
+            for (int w = 0; w < NWP; ++w) sum += s_wps[w][tid];
+            s_psum[tid] = sum;
+        }
+
+        const int lr = tid % LPR;
+        const int rg = tid / LPR;
+        float acc[G][EPC];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) acc[h][e] = 0.f;
+        for (int r = rg; r < npg * P; r += RG) {
+            float w[G];
+            bool any = false;
+#pragma unroll
+            for (int h = 0; h < G; ++h) { w[h] = s_w[r * G + h]; any |= w[h] > 0.f; }
+            if (!any) continue;
+            float x[EPC];
+            Elem<T>::widen(*reinterpret_cast<const uint4*>(stage + (size_t)r * D + lr * EPC), x);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc[h][e] = fmaf(w[h], x[e], acc[h][e]);
+        }
+        __syncthreads();   // the stage area becomes the reduction buffer
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) s_red[((size_t)rg * G + h) * D + lr * EPC + e] = acc[h][e];
+        __syncthreads();
+        if (nchunks == 1) {
+            for (int i = tid; i < G * D; i += blockDim.x) {
+                float so = 0.f;
+                for (int g = 0; g < RG; ++g) so += s_red[(size_t)g * G * D + i];
+                const float sp = s_psum[i / D];
+                outb[i] = sp > 0.f ? so / sp : 0.f;
+            }
+        } else {
+            float* part = ws.partial + ((int64_t)u * L.SmaxV + c) * G * (D + 1);
+            for (int i = tid; i < G * D; i += blockDim.x) {
+                float so = 0.f;
+                for (int g = 0; g < RG; ++g) so += s_red[(size_t)g * G * D + i];
+                part[i] = so;
+            }
+            if (tid < G) part[G * D + tid] = s_psum[tid];
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) s_last = atomicAdd(&ws.counter[u], 1) == nchunks - 1;
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                const float* part0 = ws.partial + (int64_t)u * L.SmaxV * G * (D + 1);
+                for (int i = tid; i < G * D; i += blockDim.x) {
+                    const int h = i / D;
+                    float so = 0.f, sp = 0.f;
+                    for (int cc = 0; cc < nchunks; ++cc) {
+                        const float* pc = part0 + (int64_t)cc * G * (D + 1);
+                        so += __ldcg(pc + i);
+                        sp += __ldcg(pc + G * D + h);
+                    }
+                    outb[i] = sp > 0.f ? so / sp : 0.f;
+                }
+                if (tid == 0) ws.counter[u] = 0;
+            }
+        }
+        // the next item's bulk copies overwrite the reduction buffer: order
+        // this thread's shared-memory writes before those async-proxy writes
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
     }
-    if (tid == 0) ws.counter[u] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -668,8 +1034,15 @@ void set_decode_stage_events(const cudaEvent_t* events, int n) {
     for (int i = 0; i < g_n_stage_events; ++i) g_stage_events[i] = events[i];
 }
 
+// Under stream capture the marks become event-record nodes of the graph
+// (external records), so a replayed graph still times its stages.
 static void stage_mark(int i, cudaStream_t s) {
-    if (g_n_stage_events) cudaEventRecord(g_stage_events[i], s);
+    if (!g_n_stage_events) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(g_stage_events[i], s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(g_stage_events[i], s);
 }
 
 cudaError_t read_decode_counts(const void* ws_base, const DecodeLayout& L, int32_t* union_pages,
@@ -684,89 +1057,96 @@ cudaError_t read_decode_counts(const void* ws_base, const DecodeLayout& L, int32
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return e;
 }
+
+static int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+    int v = 148;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && dev < 64) cached[dev] = v;
+    return v;
+}
+
+template <int E, typename T, int D, int G>
+static cudaError_t launch_tau_pv(float alpha, int Hq, const KV& kv, const WS& ws,
+                                 const DecodeLayout& L, int cap, float* out, float* tau_out,
+                                 int32_t* support_out, cudaStream_t s) {
+    const int cand_cap = cap * kv.P;
+    const size_t tsmem = (size_t)cand_cap * 8 + (size_t)L.nbw * 4;
+    cudaError_t e = cudaFuncSetAttribute(tau_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tsmem);
+    if (e != cudaSuccess) return e;
+    stage_mark(2, s);
+    tau_kernel<E><<<kv.B * Hq, kTauThreads, tsmem, s>>>(Hq, kv.P, alpha, cand_cap, ws, L, tau_out,
+                                                         support_out);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    constexpr int EPC = Elem<T>::kPer16;
+    constexpr int RG = kPvThreads / (D / EPC);
+    const size_t page_bytes = (size_t)kv.P * D * sizeof(T);
+    const int chv = (int)std::max<size_t>(L.CHV, std::min<size_t>(kPvMaxChunk, kPvStageBytes / page_bytes));
+    const size_t stage_bytes = std::max((size_t)chv * page_bytes, (size_t)RG * G * D * sizeof(float));
+    const size_t psmem = stage_bytes + (size_t)chv * kv.P * G * sizeof(float) +
+                         (size_t)(2 * L.U + 1) * sizeof(int);
+    e = cudaFuncSetAttribute(pv_kernel<T, D, G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)psmem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(sm_count());
+    stage_mark(3, s);
+    pv_kernel<T, D, G, E><<<grid, kPvThreads, psmem, s>>>(Hq, alpha, kv, ws, L, out, chv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    stage_mark(4, s);
+    return cudaSuccess;
+}
+
 template <typename T, int D, int G>
 static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV& kv,
                                    const int32_t* sel, const int32_t* n_sel, int cap, float alpha,
                                    float* out, float* tau_out, int32_t* support_out, const WS& ws,
                                    const DecodeLayout& L, cudaStream_t s) {
     cudaError_t e;
-    // plan
+    if (L.U > kMaxUnits || L.nbw > kPvThreads) return cudaErrorInvalidValue;
     {
         const int nwm = (kv.maxp + 31) / 32;
-        const size_t smem = (size_t)(2 * G + 1) * nwm * 4;
-        e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+        const size_t smem = (size_t)G * nwm * 4;
+        e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         stage_mark(0, s);
         plan_kernel<G><<<L.U, kPlanThreads, smem, s>>>(kv, Hq, sel, n_sel, cap, ws, L);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    // qk
-    {
-        using S = QkShape<D, G, T>;
-        const int sp = std::max(1, S::TPP / kv.P);
-        const size_t stage_bytes = (size_t)sp * kv.P * D * sizeof(T);
-        const int nst = (int)std::max<size_t>(2, std::min<size_t>(8, (64 * 1024) / stage_bytes));
-        const size_t smem = stage_bytes * nst;
-        e = cudaFuncSetAttribute(qk_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+    if constexpr (sizeof(T) == 2) {
+        const int page_bytes = kv.P * D * 2;
+        const int ns = std::min(8, kQmStageBytes / page_bytes);
+        const size_t smem = (size_t)kQmWarps * ns * page_bytes + (size_t)(L.U + 1) * sizeof(int);
+        if (ns < 2) return cudaErrorInvalidValue;
+        e = cudaFuncSetAttribute(qk_mma_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        dim3 grid(L.Smax, L.U);
         stage_mark(1, s);
-        qk_kernel<T, D, G><<<grid, kQkThreads, smem, s>>>(q, Hq, (alpha - 1.f) * scale, kv, ws, L,
-                                                          sp, nst);
+        qk_mma_kernel<D, G><<<sm_count() * kQmCtasPerSm, kQmWarps * 32, smem, s>>>(
+            q, Hq, (alpha - 1.f) * scale, kv, ws, L, ns);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    // tau
-    {
-        int M = 1;
-        while (M < L.zcap) M <<= 1;
-        const size_t smem = (size_t)M * sizeof(float);
-        const float a = alpha;
-        const int E = fabsf(a - 1.5f) < 1e-6f ? 2 : (fabsf(a - 2.f) < 1e-6f ? 1 : 0);
-        const dim3 grid(kv.B * Hq);
-        stage_mark(2, s);
-        if (E == 2) {
-            e = cudaFuncSetAttribute(tau_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e == cudaSuccess)
-                tau_kernel<2><<<grid, kTauThreads, smem, s>>>(alpha, kv.P, ws, L, tau_out, support_out);
-        } else if (E == 1) {
-            e = cudaFuncSetAttribute(tau_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e == cudaSuccess)
-                tau_kernel<1><<<grid, kTauThreads, smem, s>>>(alpha, kv.P, ws, L, tau_out, support_out);
-        } else {
-            e = cudaFuncSetAttribute(tau_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e == cudaSuccess)
-                tau_kernel<0><<<grid, kTauThreads, smem, s>>>(alpha, kv.P, ws, L, tau_out, support_out);
-        }
-        if (e != cudaSuccess) return e;
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        // pv
-        constexpr int EPC = Elem<T>::kPer16;
-        constexpr int RPP = (kPvThreads / 32) * (32 / (D / EPC));
+    } else {
         const size_t page_bytes = (size_t)kv.P * D * sizeof(T);
-        const int nst = (int)std::max<size_t>(2, std::min<size_t>(8, (64 * 1024) / page_bytes));
-        const size_t pv_smem = (size_t)kChunkPages * kv.P * G * 4 + (size_t)RPP * G * D * 4 +
-                               page_bytes * nst;
-        dim3 pgrid(L.Smax, L.U);
-        stage_mark(3, s);
-        if (E == 2) {
-            e = cudaFuncSetAttribute(pv_kernel<T, D, G, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pv_smem);
-            if (e == cudaSuccess)
-                pv_kernel<T, D, G, 2><<<pgrid, kPvThreads, pv_smem, s>>>(Hq, alpha, kv, ws, L, out, nst);
-        } else if (E == 1) {
-            e = cudaFuncSetAttribute(pv_kernel<T, D, G, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pv_smem);
-            if (e == cudaSuccess)
-                pv_kernel<T, D, G, 1><<<pgrid, kPvThreads, pv_smem, s>>>(Hq, alpha, kv, ws, L, out, nst);
-        } else {
-            e = cudaFuncSetAttribute(pv_kernel<T, D, G, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pv_smem);
-            if (e == cudaSuccess)
-                pv_kernel<T, D, G, 0><<<pgrid, kPvThreads, pv_smem, s>>>(Hq, alpha, kv, ws, L, out, nst);
-        }
+        const size_t fixed = (size_t)kQkConsumers * G * kv.P * 4 + (size_t)((L.U + 1 + 3) & ~3) * 4;
+        const size_t per_slot = page_bytes + sizeof(QkInfo) + 16;
+        int ns = (int)std::min<size_t>(kQkMaxSlots, (kQkSmemBudget - fixed) / per_slot);
+        ns = (ns / kQkConsumers) * kQkConsumers;
+        if (ns < kQkConsumers) return cudaErrorInvalidValue;
+        const size_t smem = fixed + (size_t)ns * per_slot;
+        e = cudaFuncSetAttribute(qk_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        stage_mark(4, s);
+        stage_mark(1, s);
+        qk_kernel<T, D, G><<<sm_count(), kQkThreads, smem, s>>>(q, Hq, (alpha - 1.f) * scale, kv, ws, L,
+                                                               ns, std::min(kQkGroup, ns));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    return cudaGetLastError();
+    const int E = fabsf(alpha - 1.5f) < 1e-6f ? 2 : (fabsf(alpha - 2.f) < 1e-6f ? 1 : 0);
+    if (E == 2) return launch_tau_pv<2, T, D, G>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
+    if (E == 1) return launch_tau_pv<1, T, D, G>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
+    return launch_tau_pv<0, T, D, G>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
 }
 
 cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, const int32_t* sel,

@@ -24,11 +24,14 @@ struct KV {
 };
 
 // Workspace of one decode call, carved from the caller's buffer.  U = B * Hkv
-// units (sequence, kv head); each unit's union of selected pages is split into
-// chunks of CH pages, one CTA per chunk.
+// units (sequence, kv head); a unit reads the union of its G heads' selected
+// pages (at most Umax of them) once.  Scores are kept per unit in union order,
+// [U][G][Umax * P], with -inf where a head did not select the page.  The value
+// stage reads only union pages holding a positive weight (a bitmap of nbw words
+// per unit), CHV of them per CTA, at most SmaxV CTAs per unit.
 struct DecodeLayout {
-    int    U, G, Umax, CH, Smax, zcap;
-    size_t union_count, head_count, counter, vpages, union_page, union_mask, union_rank;
+    int    U, G, Umax, nbw, CHV, SmaxV;
+    size_t union_count, counter, vpages, head_max, union_page, union_mask, supp;
     size_t z, tau, partial, total;
 };
 DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap);

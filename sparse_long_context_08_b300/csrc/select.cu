@@ -1,10 +1,10 @@
 // Candidate page selection [EntmaxKV §2.B].
 //
 // Top-k (§2.B.1): one CTA per (sequence, query head) holds the head's page
-// bounds as order-preserving uint32 keys in shared memory, finds the k-th
-// largest key with a 4-pass MSB radix select (8-bit digits, per-warp
-// histograms), then writes the selected pages in ascending order with two
-// block scans: ties at the k-th key go to the lower page ids.
+// bounds as order-preserving uint32 keys in shared memory, finds the boundary
+// with an MSB radix select that starts at the highest bit where the keys
+// differ, then writes the selected pages in ascending order with one block
+// scan: ties at the k-th key go to the lower page ids.
 //
 // Gaussian tau-hat (§2.B.2): one CTA per (sequence, query head) solves
 //   F(tau) = sum_p n_p E[((alpha-1) X_p - tau)_+^e] - 1 = 0,  X_p ~ N(m_p, s_p^2)
@@ -116,63 +116,158 @@ __device__ int compact_topk(const uint32_t* keys, int n, uint32_t kth, int take_
     return tot;
 }
 
-__global__ void __launch_bounds__(kSelThreads)
+// Top-k by bound: one CTA per (sequence, query head), the head's bounds as
+// order-preserving uint32 keys in shared memory.  The radix select starts at
+// the highest bit where the smallest and largest keys differ (every key shares
+// the bits above it, so no pass is wasted on them) and stops as soon as the
+// boundary bin is taken whole.  Ties at the k-th key go to the lower pages.
+constexpr int kTopkMaxThreads = 1024;
+
+__global__ void __launch_bounds__(kTopkMaxThreads)
 select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
                    int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
                    float* __restrict__ aux) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    __shared__ SelShared sh;
-    const int nw = blockDim.x >> 5;
-    int* whist = reinterpret_cast<int*>(smem_raw);
-    int* hist = whist + nw * 256;
-    uint32_t* keys = reinterpret_cast<uint32_t*>(hist + 256);
-
+    extern __shared__ __align__(16) uint32_t keys[];   // [max_pages]
+    __shared__ int hist[256];
+    __shared__ uint32_t umin_red[32], umax_red[32];
+    __shared__ int ired[40];
+    __shared__ int s_digit, s_above;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nt = blockDim.x, nwarps = nt >> 5;
     const int bh = blockIdx.x;
     const int b = bh / Hq;
-    const int len = kv.sl[b];
-    const int np = min(kv.maxp, (len + kv.P - 1) / kv.P);
+    const int np = min(kv.maxp, (kv.sl[b] + kv.P - 1) / kv.P);
     const float* src = bound + (int64_t)bh * kv.maxp;
     int32_t* dst = sel + (int64_t)bh * kp;
-    for (int i = threadIdx.x; i < np; i += blockDim.x) keys[i] = float_key(src[i]);
-    __syncthreads();
     const int k = min(kp, np);
     if (k <= 0) {
-        if (threadIdx.x == 0) {
+        if (tid == 0) {
             n_sel[bh] = 0;
             if (aux) { aux[2 * bh] = INFINITY; aux[2 * bh + 1] = -INFINITY; }
         }
         return;
     }
-    uint32_t kth;
-    int take_eq;
-    if (k == np) {
-        kth = 0;              // below every real key: take everything
-        take_eq = 0;
-    } else {
-        radix_kth(keys, np, k, whist, hist, sh, kth, take_eq);
+    uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
+    for (int i = tid; i < np; i += nt) {
+        const uint32_t key = float_key(__ldcg(src + i));
+        keys[i] = key;
+        kmn = min(kmn, key);
+        kmx = max(kmx, key);
     }
-    uint32_t next_key;
-    const int got = compact_topk(keys, np, kth, take_eq, dst, sh, &next_key);
-    if (threadIdx.x == 0) {
-        n_sel[bh] = got;
-        if (aux) {
-            float kth_f = INFINITY;
-            if (k == np) {
-                // smallest kept bound when every page is kept
-                kth_f = INFINITY;
-            } else {
-                kth_f = key_float(kth);
-            }
-            aux[2 * bh] = kth_f;
-            aux[2 * bh + 1] = k < np ? key_float(next_key) : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kmn = min(kmn, __shfl_xor_sync(0xFFFFFFFFu, kmn, o));
+        kmx = max(kmx, __shfl_xor_sync(0xFFFFFFFFu, kmx, o));
+    }
+    if (lane == 0) { umin_red[wid] = kmn; umax_red[wid] = kmx; }
+    for (int i = tid; i < 256; i += nt) hist[i] = 0;
+    __syncthreads();
+    kmn = lane < nwarps ? umin_red[lane] : 0xFFFFFFFFu;
+    kmx = lane < nwarps ? umax_red[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kmn = min(kmn, __shfl_xor_sync(0xFFFFFFFFu, kmn, o));
+        kmx = max(kmx, __shfl_xor_sync(0xFFFFFFFFu, kmx, o));
+    }
+
+    // B = {keys whose bits above `shift` equal `hi`}; everything above B is
+    // taken, and `rem` more are taken from B.
+    const uint32_t diff = kmn ^ kmx;
+    int shift = diff ? 32 - __clz(diff) : 0;
+    uint64_t hi = (uint64_t)kmx >> shift;
+    int rem = k, nB = np;
+    while (shift > 0 && nB != rem) {
+        const int dbits = min(8, shift);
+        shift -= dbits;
+        const uint32_t dmask = (1u << dbits) - 1u;
+        for (int i = tid; i < np; i += nt) {
+            const uint32_t key = keys[i];
+            if (((uint64_t)key >> (shift + dbits)) == hi) atomicAdd(&hist[(key >> shift) & dmask], 1);
         }
+        __syncthreads();
+        if (wid == 0) {
+            int lsum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) lsum += hist[lane * 8 + j];
+            int incl = lsum;       // inclusive suffix sum over lanes
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+                if (lane + o < 32) incl += v;
+            }
+            int acc = incl - lsum;
+#pragma unroll
+            for (int j = 7; j >= 0; --j) {
+                const int d = lane * 8 + j;
+                const int c = hist[d];
+                if (acc < rem && acc + c >= rem) { s_digit = d; s_above = acc; }
+                acc += c;
+            }
+        }
+        __syncthreads();
+        const int d = s_digit;
+        rem -= s_above;
+        nB = hist[d];
+        hi = (hi << dbits) | (uint64_t)d;
+        __syncthreads();
+        for (int i = tid; i < 256; i += nt) hist[i] = 0;
+        __syncthreads();
     }
-    if (k == np && aux) {
-        // every page kept: the smallest kept bound is the minimum key
-        uint32_t mn = 0xFFFFFFFFu;
-        for (int i = threadIdx.x; i < np; i += blockDim.x) mn = min(mn, keys[i]);
-        const uint32_t mx = block_max_u(~mn, sh.ured);
-        if (threadIdx.x == 0) aux[2 * bh] = key_float(~mx);
+    const int takeB = rem;    // == nB when B is taken whole
+
+    // compaction in page order: one packed scan of (above, in-B) counts
+    const int seg = (np + nt - 1) / nt;
+    const int i0 = min(np, tid * seg), i1 = min(np, i0 + seg);
+    int na = 0, nb_ = 0;
+    for (int i = i0; i < i1; ++i) {
+        const uint64_t kh = (uint64_t)keys[i] >> shift;
+        na += kh > hi;
+        nb_ += kh == hi;
+    }
+    // both counts are below 2^16 (max_pages <= 49152): the packed sum fits
+    // 32 unsigned bits
+    int tot;
+    const uint32_t ex = static_cast<uint32_t>(block_exclusive_scan((na << 16) | nb_, ired, &tot));
+    int a = static_cast<int>(ex >> 16), r = static_cast<int>(ex & 0xFFFFu);
+    uint32_t tmin = 0xFFFFFFFFu, nmax = 0u;
+    bool any_out = false;
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t key = keys[i];
+        const uint64_t kh = (uint64_t)key >> shift;
+        bool take = false;
+        if (kh > hi) {
+            dst[a + min(r, takeB)] = i;
+            ++a;
+            take = true;
+        } else if (kh == hi) {
+            if (r < takeB) {
+                dst[a + r] = i;
+                take = true;
+            }
+            ++r;
+        }
+        if (take) tmin = min(tmin, key);
+        else { nmax = max(nmax, key); any_out = true; }
+    }
+    // smallest taken key (the k-th bound) and largest key left out
+    const int any = __syncthreads_or(any_out);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        tmin = min(tmin, __shfl_xor_sync(0xFFFFFFFFu, tmin, o));
+        nmax = max(nmax, __shfl_xor_sync(0xFFFFFFFFu, nmax, o));
+    }
+    if (lane == 0) { umin_red[wid] = tmin; umax_red[wid] = nmax; }
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 1; w < nwarps; ++w) {
+            tmin = min(tmin, umin_red[w]);
+            nmax = max(nmax, umax_red[w]);
+        }
+        n_sel[bh] = k;
+        if (aux) {
+            aux[2 * bh] = key_float(tmin);
+            aux[2 * bh + 1] = any ? key_float(nmax) : -INFINITY;
+        }
     }
 }
 
@@ -311,9 +406,9 @@ static int max_optin_smem() {
 
 cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp, int32_t* sel,
                                int32_t* n_sel, float* aux, cudaStream_t s) {
-    const int threads = kSelThreads;
-    const size_t smem = (size_t)(threads / 32) * 256 * 4 + 256 * 4 + (size_t)kv.maxp * 4;
-    if ((int)smem > max_optin_smem() - (int)sizeof(SelShared)) return cudaErrorInvalidValue;
+    const int threads = kv.maxp <= 8192 ? 256 : (kv.maxp <= 16384 ? 512 : 1024);
+    const size_t smem = (size_t)kv.maxp * 4;
+    if ((int)smem > max_optin_smem() - 4096) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -31,7 +31,7 @@ if ROOT not in sys.path:
 
 METRIC = "sparse entmax decode µs/step and achieved HBM GB/s (frac of peak) at 128K ctx"
 FALLBACK_HBM_GBS = 6400.0
-KERNELS_PER_STEP = 6   # score, select, plan, qk, tau, pv
+KERNELS_PER_STEP = 5   # score, select, plan, qk, tpv (threshold + values)
 
 
 def parse():
@@ -248,8 +248,8 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     # the step is replayed as a CUDA graph; event-record nodes at the stage
-    # boundaries time score | select | plan | qk | tau | pv on the device
-    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)]
+    # boundaries time score | select | plan | qk | tpv on the device
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
     for x in evs:
         x.record()             # materialise the events before capture
     torch.cuda.synchronize()
@@ -266,7 +266,7 @@ def run_ours(args):
         dec.score(q)
         evs[1].record()
         dec.select()
-        E.entmaxkv_set_stage_events(evs[2:7])
+        E.entmaxkv_set_stage_events(evs[2:6])
         dec.decode(q)
         E.entmaxkv_set_stage_events(None)
     torch.cuda.synchronize()
@@ -279,7 +279,7 @@ def run_ours(args):
         dist.barrier()
 
     K = args.steps
-    names = ["score", "select", "plan", "qk", "tau", "pv"]
+    names = ["score", "select", "plan", "qk", "tpv"]
     stage = {n: [] for n in names}
     total = []
     sampler = ClockSampler(bus_id_of(local_rank)) if rank == 0 else None
@@ -288,10 +288,10 @@ def run_ours(args):
     for i in range(K):
         graph.replay()
         torch.cuda.synchronize()
-        t = [evs[j].elapsed_time(evs[j + 1]) for j in range(6)]
+        t = [evs[j].elapsed_time(evs[j + 1]) for j in range(5)]
         for n_, v in zip(names, t):
             stage[n_].append(v)
-        total.append(evs[0].elapsed_time(evs[6]))
+        total.append(evs[0].elapsed_time(evs[5]))
         flush_l2(i + 7)                     # L2 flush between steps, outside the events
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
@@ -301,7 +301,7 @@ def run_ours(args):
     ms_per_step = float(t_sum.item()) / K
 
     # bytes the step reads (metadata + selected pages + small tensors)
-    up, vp = E.entmaxkv_decode_counts(dec.workspace, w.batch, w.num_q_heads, w.num_kv_heads,
+    up, vr = E.entmaxkv_decode_counts(dec.workspace, w.batch, w.num_q_heads, w.num_kv_heads,
                                       w.head_dim, w.page_size, w.max_pages, dec.cap)
     esz = 2 if w.dtype == "bf16" else 4
     pages = sum(w.pages_of(b) for b in range(w.batch))
@@ -309,11 +309,11 @@ def run_ours(args):
     meta_row = 2 * w.head_dim * (esz if w.policy == "topk" else 4)
     bytes_meta = pages * w.num_kv_heads * meta_row + pages * 4
     bytes_k = int(up.sum()) * page_bytes
-    bytes_v = int(vp.sum()) * page_bytes
+    bytes_v = int(vr.sum()) * w.head_dim * esz
     small = 2 * w.batch * w.num_q_heads * w.head_dim * 4
     bytes_step = bytes_meta + bytes_k + bytes_v + small
     mean = {n: statistics.mean(v) for n, v in stage.items()}
-    per_kernel_bytes = {"score": bytes_meta, "qk": bytes_k, "pv": bytes_v}
+    per_kernel_bytes = {"score": bytes_meta, "qk": bytes_k, "tpv": bytes_v}
     dom = max(mean, key=mean.get)
     peak, peak_kind = measured_peak()
     dom_bytes = per_kernel_bytes.get(dom)
@@ -380,8 +380,8 @@ def run_ours(args):
         "hbm_frac_of_8tbs": bytes_step / (ms_per_step * 1e-3) / 1e9 / 8000.0,
         "bytes_per_step": bytes_step,
         "bytes_breakdown": {"metadata_and_page_table": bytes_meta, "k_union_pages": bytes_k,
-                            "v_support_pages": bytes_v, "q_and_out": small,
-                            "union_pages": int(up.sum()), "v_pages": int(vp.sum())},
+                            "v_support_rows": bytes_v, "q_and_out": small,
+                            "union_pages": int(up.sum()), "v_rows": int(vr.sum())},
         "stage_us": {n: v * 1e3 for n, v in mean.items()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": KERNELS_PER_STEP * K, "clocks": clocks,

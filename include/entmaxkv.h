@@ -139,10 +139,10 @@ int entmaxkv_select(const float* page_scores, const ekv_paged_kv* kv,
  * For each (b, h): the valid tokens of pages sel[b, h, 0:n_sel[b, h]] (distinct
  * ids, any order, each < ceil(seq_lens[b] / page_size); duplicates count once)
  * are scored z = scale q.k, tau is the exact alpha-entmax threshold of
- * (alpha-1) z over them (closed form after a sort for alpha 1.5 and 2,
- * bisection otherwise), and out = sum_i p_i v_i / sum_i p_i.  Each kv head's
- * K page is read once per step for its whole query group; V pages holding no
- * token with p_i > 0 for any head of the group are not read.
+ * (alpha-1) z over them (Newton from the left for alpha 1.5 and 2, bisection
+ * otherwise), and out = sum_i p_i v_i / sum_i p_i.  Each kv head's K page is
+ * read once per step for its whole query group; only the V rows of tokens with
+ * p_i > 0 are read.
  * tau_out (nullable) fp32 [batch, num_q_heads] in (alpha-1) z units; support_out
  * (nullable) int32 [batch, num_q_heads] = #{p_i > 0}.  An empty selection gives
  * out = 0, tau = +inf, support 0.  alpha > 1.  workspace: device scratch of at
@@ -197,24 +197,26 @@ const char* entmaxkv_status_string(int32_t status);
  * Returns EKV_CUDA_ERROR if the copy fails. */
 int entmaxkv_read_device_status(int32_t* status_out /* host */, void* stream);
 
-/* Measurement aid (not part of the method): record five caller-created
+/* Measurement aid (not part of the method): record four caller-created
  * cudaEvent_t handles around the kernels of every later entmaxkv_decode call on
  * its stream: events[0] before the union plan, [1] before the score kernel,
- * [2] before the threshold kernel, [3] before the value kernel, [4] after it.
- * n_events = 0 (events may be NULL) turns it off.  Process-wide, not
- * thread-safe; the events must outlive every decode call made while set. */
+ * [2] before the threshold-and-value kernel, [3] after it.  n_events = 0
+ * (events may be NULL) turns it off.  Under stream capture the events become
+ * external event-record nodes of the graph.  Process-wide, not thread-safe;
+ * the events must outlive every decode call made while set. */
 int entmaxkv_set_stage_events(void* const* events /* host array */, int32_t n_events);
 
 /* Measurement aid: after an entmaxkv_decode that used `workspace` (same sizes),
  * copy per (sequence, kv head) unit the number of distinct pages whose K was
- * read (the union of the group's selections) and whose V was read (union pages
- * holding a token with p > 0 for some head of the group) into the HOST arrays
- * union_pages and v_pages (int32 [batch * num_kv_heads], either nullable).
- * Synchronises `stream`. */
-int entmaxkv_decode_counts(const void* workspace, int32_t batch, int32_t num_q_heads,
+ * read (the union of the group's selections) and the number of distinct tokens
+ * whose V row was read (tokens with p > 0 for some head of the group) into the
+ * HOST arrays union_pages and v_rows (int32 [batch * num_kv_heads], either
+ * nullable).  Writes a per-unit count field of the workspace (one small kernel)
+ * and synchronises `stream`. */
+int entmaxkv_decode_counts(void* workspace, int32_t batch, int32_t num_q_heads,
                            int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                            int32_t max_pages, int32_t cap_pages, int32_t* union_pages,
-                           int32_t* v_pages, void* stream);
+                           int32_t* v_rows, void* stream);
 
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 int32_t entmaxkv_version(void);

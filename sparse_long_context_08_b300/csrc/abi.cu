@@ -144,10 +144,10 @@ int entmaxkv_select(const float* page_scores, const ekv_paged_kv* kv, int32_t nu
     return EKV_INVALID_ARG;
 }
 
-int entmaxkv_decode(const float* q, int32_t num_q_heads, float scale, const ekv_paged_kv* kv,
-                    const int32_t* sel, const int32_t* n_sel, int32_t cap_pages, float alpha,
-                    float* out, float* tau_out, int32_t* support_out, void* workspace,
-                    size_t ws_bytes, void* stream) {
+static int decode_impl(const float* q, int32_t num_q_heads, float scale, const ekv_paged_kv* kv,
+                       const int32_t* sel, const int32_t* n_sel, int32_t cap_pages, float alpha,
+                       float* out, float* tau_out, int32_t* support_out, void* workspace,
+                       size_t ws_bytes, void* stream) {
     int st = check_kv(kv, true, true);
     if (st) return st;
     if ((st = check_heads(kv, num_q_heads))) return st;
@@ -157,6 +157,7 @@ int entmaxkv_decode(const float* q, int32_t num_q_heads, float scale, const ekv_
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EKV_INVALID_ARG;
     if ((int64_t)cap_pages * kv->page_size > 16384) return EKV_UNSUPPORTED;
     if ((int64_t)kv->max_pages > ekv::kMaxPagesTopk) return EKV_UNSUPPORTED;
+    if ((int64_t)kv->num_blocks * kv->num_kv_heads * kv->page_size > INT32_MAX) return EKV_UNSUPPORTED;
     const ekv::DecodeLayout L = ekv::decode_layout(kv->batch, num_q_heads, kv->num_kv_heads,
                                                    kv->head_dim, kv->page_size, kv->max_pages,
                                                    cap_pages);
@@ -166,22 +167,30 @@ int entmaxkv_decode(const float* q, int32_t num_q_heads, float scale, const ekv_
                                         static_cast<cudaStream_t>(stream)));
 }
 
+int entmaxkv_decode(const float* q, int32_t num_q_heads, float scale, const ekv_paged_kv* kv,
+                    const int32_t* sel, const int32_t* n_sel, int32_t cap_pages, float alpha,
+                    float* out, float* tau_out, int32_t* support_out, void* workspace,
+                    size_t ws_bytes, void* stream) {
+    return decode_impl(q, num_q_heads, scale, kv, sel, n_sel, cap_pages, alpha, out, tau_out,
+                       support_out, workspace, ws_bytes, stream);
+}
+
 int entmaxkv_set_stage_events(void* const* events, int32_t n_events) {
-    if (n_events != 0 && (n_events != 5 || !events)) return EKV_INVALID_ARG;
+    if (n_events != 0 && (n_events != 4 || !events)) return EKV_INVALID_ARG;
     ekv::set_decode_stage_events(reinterpret_cast<const cudaEvent_t*>(events), n_events);
     return EKV_OK;
 }
 
-int entmaxkv_decode_counts(const void* workspace, int32_t batch, int32_t num_q_heads,
+int entmaxkv_decode_counts(void* workspace, int32_t batch, int32_t num_q_heads,
                            int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                            int32_t max_pages, int32_t cap_pages, int32_t* union_pages,
-                           int32_t* v_pages, void* stream) {
+                           int32_t* v_rows, void* stream) {
     if (!workspace || entmaxkv_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
                                               page_size, max_pages, cap_pages) == 0)
         return EKV_INVALID_ARG;
     const ekv::DecodeLayout L = ekv::decode_layout(batch, num_q_heads, num_kv_heads, head_dim,
                                                    page_size, max_pages, cap_pages);
-    return from_cuda(ekv::read_decode_counts(workspace, L, union_pages, v_pages,
+    return from_cuda(ekv::read_decode_counts(workspace, L, union_pages, v_rows,
                                              static_cast<cudaStream_t>(stream)));
 }
 

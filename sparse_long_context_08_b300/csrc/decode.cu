@@ -6,36 +6,30 @@
 //   plan  (1 CTA per unit)      bitmaps of each head's pages -> union list in
 //                               ascending page order with a per-page head mask;
 //                               resets the unit's per-call state.
-//   qk    (persistent, 1 CTA    the flattened union lists of all units are cut
-//          per SM)              into one contiguous range per CTA.  A producer
-//                               warp resolves page-table entries and bulk-copies
-//                               K pages (cp.async.bulk) into a ring of slots;
-//                               each consumer warp owns a fixed subset of the
-//                               slots and turns a page into z' = (alpha-1) s q.k
-//                               for the G heads with fp32 FMA (G <= 8 query rows
-//                               cannot fill a tensor-core tile), reduced across
-//                               lanes by a transposing butterfly.  Scores are
-//                               stored per unit in union order, -inf where a head
-//                               did not select the page; per-head maxima go out
-//                               through atomics.
-//   tau   (1 CTA per head)      candidates z' > max - 1 (all others have zero
-//                               weight) are compacted in index order; tau solves
+//   qk                          the flattened union lists of all units are cut
+//                               into one contiguous range per warp; K pages go
+//                               through a private ring of bulk copies per warp
+//                               and z' = (alpha-1) s q.k is computed for the G
+//                               heads (bf16 K: tensor cores, see qk_mma_kernel;
+//                               fp32 K: FMA).  Scores are stored per unit in
+//                               union order, -inf where a head did not select
+//                               the page; per-head maxima go out through atomics
+//                               and each page's physical block is recorded.
+//   tpv   (1 CTA per head)      candidates z' > max - 1 (all others have zero
+//                               weight) are compacted; tau solves
 //                               sum (z' - tau)_+^(1/(alpha-1)) = 1 by Newton from
 //                               the left (alpha 1.5 and 2: the function is convex,
 //                               so the iterates rise monotonically to the root)
-//                               or by bisection (other alpha).  The pages holding
-//                               the support are marked in a per-unit bitmap.
-//   pv    (chunks of marked     V pages with no positive weight are never read.
-//          pages per CTA)       p = (z' - tau)_+^(1/(alpha-1)); out = sum p v /
-//                               sum p.  A unit whose support pages fit one CTA
-//                               writes out directly; otherwise the chunks' partial
-//                               sums are merged in a fixed order by the unit's
-//                               last CTA (tau is global, so the merge is a sum).
+//                               or by bisection (other alpha); then only the V
+//                               rows of the support tokens are read and
+//                               out = sum p v / sum p.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
 
 EKV_DEFINE_STATUS(decode)
+
+#include "plan.cuh"
 
 namespace ekv {
 
@@ -46,63 +40,32 @@ constexpr int kQkGroup = 16;                           // pages resolved per pro
 constexpr int kQkMaxSlots = 48;
 constexpr int kQkSmemBudget = 220 * 1024;
 constexpr int kMaxUnits = 8192;                        // qk keeps a prefix over units in smem
-constexpr int kTauThreads = 512;
-constexpr int kPvThreads = 256;
-constexpr int kPvMaxChunk = 16;                        // support pages per pv CTA
-constexpr int kPvStageBytes = 128 * 1024;
+constexpr int kTpvThreads = 256;
+constexpr int kTpvVec = 8;                             // float4 per thread per score tile
+constexpr int kTpvTile = kTpvThreads * kTpvVec * 4;    // scores per tile
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap) {
+    (void)D;
     DecodeLayout L{};
     L.U = B * Hkv;
     L.G = Hq / Hkv;
     L.Umax = std::min(L.G * cap, max_pages);
-    L.nbw = (L.Umax + 31) / 32;
-    // chunk size of the value stage, sized for fp32 pages (the largest); bf16
-    // launches use chunks at least this large, hence never more of them
-    L.CHV = std::max(1, std::min(kPvMaxChunk, kPvStageBytes / (P * D * 4)));
-    L.SmaxV = (L.Umax + L.CHV - 1) / L.CHV;
+    L.nvw = (L.Umax * P + 31) / 32;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
     L.union_count = take(sizeof(int) * L.U);
-    L.counter = take(sizeof(int) * L.U);
-    L.vpages = take(sizeof(int) * L.U);
     L.head_max = take(sizeof(uint32_t) * (size_t)B * Hq);
     L.union_page = take(sizeof(int) * (size_t)L.U * L.Umax);
     L.union_mask = take(sizeof(int) * (size_t)L.U * L.Umax);
-    L.supp = take(sizeof(uint32_t) * (size_t)L.U * L.nbw);
+    L.union_blk = take(sizeof(int) * (size_t)L.U * L.Umax);
+    L.vtok = take(sizeof(uint32_t) * (size_t)L.U * L.nvw);
+    L.vrows = take(sizeof(int) * L.U);
     L.z = take(sizeof(float) * (size_t)L.U * L.G * L.Umax * P);
     L.tau = take(sizeof(float) * (size_t)B * Hq);
-    L.partial = take(sizeof(float) * (size_t)L.U * L.SmaxV * L.G * (D + 1));
     L.total = o;
     return L;
-}
-
-// Workspace views (device addresses).
-struct WS {
-    int* union_count;
-    int* counter;
-    int* vpages;
-    uint32_t* head_max;   // order-preserving keys of each head's max z'
-    int* union_page;
-    int* union_mask;
-    uint32_t* supp;       // [U][nbw] union pages holding a positive weight
-    float* z;             // [U][G][Umax * P]
-    float* tau;
-    float* partial;
-};
-static WS ws_views(void* base, const DecodeLayout& L) {
-    char* c = static_cast<char*>(base);
-    return WS{reinterpret_cast<int*>(c + L.union_count), reinterpret_cast<int*>(c + L.counter),
-              reinterpret_cast<int*>(c + L.vpages), reinterpret_cast<uint32_t*>(c + L.head_max),
-              reinterpret_cast<int*>(c + L.union_page), reinterpret_cast<int*>(c + L.union_mask),
-              reinterpret_cast<uint32_t*>(c + L.supp), reinterpret_cast<float*>(c + L.z),
-              reinterpret_cast<float*>(c + L.tau), reinterpret_cast<float*>(c + L.partial)};
-}
-
-__device__ __forceinline__ int pages_of(const KV& kv, int b) {
-    return min(kv.maxp, (kv.sl[b] + kv.P - 1) / kv.P);
 }
 
 // ---------------------------------------------------------------------------
@@ -112,70 +75,12 @@ template <int G>
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(KV kv, int Hq, const int32_t* __restrict__ sel, const int32_t* __restrict__ n_sel,
             int cap, WS ws, DecodeLayout L) {
-    extern __shared__ __align__(16) uint32_t s_bits[];   // [G][nwm]
+    extern __shared__ __align__(16) uint32_t s_plan[];   // bitmaps, then union pages
     __shared__ int red[40];
+    __shared__ int s_ns[G];
     const int nwm = (kv.maxp + 31) / 32;
-    const int u = blockIdx.x;
-    const int b = u / kv.hkv;
-    const int kvh = u - b * kv.hkv;
-    const int np = pages_of(kv, b);
-    const int nw = (np + 31) / 32;
-    const int tid = threadIdx.x;
-
-    for (int i = tid; i < G * nw; i += blockDim.x) {
-        const int h = i / nw;
-        s_bits[h * nwm + (i - h * nw)] = 0u;
-    }
-    // per-call state the later stages accumulate into
-    if (tid < G) ws.head_max[b * Hq + kvh * G + tid] = 0u;
-    for (int i = tid; i < L.nbw; i += blockDim.x) ws.supp[(int64_t)u * L.nbw + i] = 0u;
-    if (tid == 0) ws.counter[u] = 0;
-    __syncthreads();
-    for (int h = 0; h < G; ++h) {
-        const int bh = b * Hq + kvh * G + h;
-        int ns = n_sel[bh];
-        if (ns < 0 || ns > cap) {
-            if (tid == 0) flag_bad_data();
-            ns = max(0, min(ns, cap));
-        }
-        for (int r = tid; r < ns; r += blockDim.x) {
-            const int p = sel[(int64_t)bh * cap + r];
-            if (p >= 0 && p < np) atomicOr(&s_bits[h * nwm + (p >> 5)], 1u << (p & 31));
-            else flag_bad_data();
-        }
-    }
-    __syncthreads();
-
-    const int seg = (nw + blockDim.x - 1) / blockDim.x;
-    const int w0 = min(nw, tid * seg), w1 = min(nw, w0 + seg);
-    int cnt = 0;
-    for (int w = w0; w < w1; ++w) {
-        uint32_t x = 0;
-#pragma unroll
-        for (int h = 0; h < G; ++h) x |= s_bits[h * nwm + w];
-        cnt += __popc(x);
-    }
-    int total;
-    int idx = block_exclusive_scan(cnt, red, &total);
-    int* upage = ws.union_page + (int64_t)u * L.Umax;
-    int* umask = ws.union_mask + (int64_t)u * L.Umax;
-    for (int w = w0; w < w1; ++w) {
-        uint32_t hw[G];
-        uint32_t uw = 0;
-#pragma unroll
-        for (int h = 0; h < G; ++h) { hw[h] = s_bits[h * nwm + w]; uw |= hw[h]; }
-        while (uw) {
-            const int bit = __ffs(uw) - 1;
-            uw &= uw - 1;
-            int mask = 0;
-#pragma unroll
-            for (int h = 0; h < G; ++h) mask |= static_cast<int>((hw[h] >> bit) & 1u) << h;
-            upage[idx] = w * 32 + bit;
-            umask[idx] = mask;
-            ++idx;
-        }
-    }
-    if (tid == 0) ws.union_count[u] = total;
+    build_plan<G>(kv, Hq, sel, n_sel, cap, ws, L, blockIdx.x, s_plan,
+                  reinterpret_cast<int*>(s_plan + (size_t)G * nwm), red, s_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -292,14 +197,11 @@ qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, Decod
                 const int idx = uu * L.Umax + ii;
                 const int page = ws.union_page[idx];
                 const int mask = ws.union_mask[idx];
+                const int blk = ws.union_blk[idx];         // validated by the plan
                 const int b = uu / kv.hkv;
                 const int kvh = uu - b * kv.hkv;
-                const int blk = kv.pt[(int64_t)b * kv.maxp + page];
                 int valid = min(P, kv.sl[b] - page * P);
-                if (blk < 0 || blk >= kv.nb) {
-                    flag_bad_data();
-                    valid = 0;
-                }
+                if (blk < 0) valid = 0;
                 const int slot = k % nslots;
                 const int use = k / nslots;
                 if (use > 0 && !mbar_wait(&empty[slot], (uint32_t)((use - 1) & 1))) {
@@ -471,17 +373,12 @@ __device__ __forceinline__ PgDesc resolve_page(int f, int f1, const int* prefix,
     d.u = lo;
     d.i = f - prefix[lo];
     const int idx = lo * L.Umax + d.i;
+    // one round trip: page, head mask and the block the plan validated
     const int page = __ldcg(ws.union_page + idx);
     d.mask = __ldcg(ws.union_mask + idx);
+    d.blk = __ldcg(ws.union_blk + idx);
     const int b = lo / kv.hkv;
-    int blk = kv.pt[(int64_t)b * kv.maxp + page];
-    d.valid = min(kv.P, kv.sl[b] - page * kv.P);
-    if (blk < 0 || blk >= kv.nb) {
-        flag_bad_data();
-        blk = -1;
-        d.valid = 0;
-    }
-    d.blk = blk;
+    d.valid = d.blk >= 0 ? min(kv.P, kv.sl[b] - page * kv.P) : 0;
     return d;
 }
 
@@ -534,9 +431,11 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
     const int npg = f1 - f0;
     if (npg <= 0) return;
     const unsigned char* kbase = static_cast<const unsigned char*>(kv.k);
+    const uint64_t evict_first = l2_evict_first_policy();
 
     PgDesc cur = resolve_page(f0 + lane, f1, s_prefix, kv, ws, L);
-    PgDesc nxt = resolve_page(f0 + 32 + lane, f1, s_prefix, kv, ws, L);
+    PgDesc nxt{-1, 0, 0, 0, 0};
+    if (npg > 32) nxt = resolve_page(f0 + 32 + lane, f1, s_prefix, kv, ws, L);
     int cur_base = 0;
     // Issues page k into stage k % ns; returns its descriptor.
     auto issue = [&](int k) -> PgDesc {
@@ -545,16 +444,16 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
         if (k >= cur_base + 32) {
             cur = nxt;
             cur_base += 32;
-            nxt = resolve_page(f0 + cur_base + 32 + lane, f1, s_prefix, kv, ws, L);
+            if (npg > cur_base + 32) nxt = resolve_page(f0 + cur_base + 32 + lane, f1, s_prefix, kv, ws, L);
         }
         dsc = shfl_desc(cur, k - cur_base);
         if (lane == 0) {
             const int st = k % ns;
             if (dsc.blk >= 0) {
                 mbar_arrive_expect_tx(&bar[st], page_bytes);
-                bulk_g2s(ring + (size_t)st * page_bytes,
-                         kbase + (((int64_t)dsc.blk * kv.hkv + dsc.u % kv.hkv) * P * D) * 2,
-                         page_bytes, &bar[st]);
+                bulk_g2s_hint(ring + (size_t)st * page_bytes,
+                              kbase + (((int64_t)dsc.blk * kv.hkv + dsc.u % kv.hkv) * P * D) * 2,
+                              page_bytes, &bar[st], evict_first);
             } else {
                 mbar_arrive(&bar[st]);
             }
@@ -676,33 +575,55 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
 }
 
 // ---------------------------------------------------------------------------
-// tau: exact alpha-entmax threshold per query head
+// tpv: exact alpha-entmax threshold and value accumulation, one CTA per head
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float pow_e(float a, int E, float ex) {
     return E == 2 ? a * a : (E == 1 ? a : powf(a, ex));
 }
 
-template <int E>   // 2: alpha = 1.5, 1: alpha = 2, 0: any other alpha
-__global__ void __launch_bounds__(kTauThreads)
-tau_kernel(int Hq, int P, float alpha, int cand_cap, WS ws, DecodeLayout L,
-           float* __restrict__ tau_out, int32_t* __restrict__ support_out) {
-    extern __shared__ __align__(16) float s_x[];     // [cand_cap] values, then positions, bitmap
-    int* s_pos = reinterpret_cast<int*>(s_x + cand_cap);
-    uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_pos + cand_cap);
+template <typename T, int D, int E>   // E: 2 alpha = 1.5, 1 alpha = 2, 0 any other alpha
+__global__ void __launch_bounds__(kTpvThreads)
+tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
+           float* __restrict__ out, float* __restrict__ tau_out, int32_t* __restrict__ support_out) {
+    constexpr int EPC = Elem<T>::kPer16;
+    constexpr int LPR = D / EPC;              // lanes per V row
+    constexpr int RG = kTpvThreads / LPR;     // V rows per pass
+    extern __shared__ __align__(16) float s_x[];                      // [cand_cap] x, then weights
+    int* s_pos = reinterpret_cast<int*>(s_x + cand_cap);              // [cand_cap] score index, then V row
+    float* s_red = reinterpret_cast<float*>(s_pos + cand_cap);        // [RG][D]
     __shared__ float fred[40];
     __shared__ float2 f2red[32];
     __shared__ int ired[40];
+    __shared__ float s_t;
 
-    const int bh = blockIdx.x;
     const int G = L.G;
+    const int Hkv = Hq / G;
+    const int bh = blockIdx.x;
     const int b = bh / Hq;
     const int h = bh - b * Hq;
-    const int u = b * (Hq / G) + h / G;
-    const int hg = h % G;
-    const int tid = threadIdx.x;
-    const uint32_t key = ws.head_max[bh];
-    const int n = ws.union_count[u] * P;
+    const int kvh = h / G;
+    const int hg = h - kvh * G;
+    const int u = b * Hkv + kvh;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int P = kv.P;
+    const int zn = L.Umax * P;
+    const float* z = ws.z + ((int64_t)u * G + hg) * zn;
+    float* outb = out + (int64_t)bh * D;
+
+    // one round trip: the head's max, the union size and the first score tile
+    const uint32_t key = __ldcg(ws.head_max + bh);
+    const int ucnt = __ldcg(ws.union_count + u);
+    float v[kTpvVec * 4];
+#pragma unroll
+    for (int j = 0; j < kTpvVec; ++j) {
+        const int i = (j * kTpvThreads + tid) * 4;     // zn is a multiple of 4
+        const float4 f = i < zn ? __ldcg(reinterpret_cast<const float4*>(z + i))
+                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+    }
+    const int n = ucnt * P;
     if (key == 0u || n == 0) {
+        for (int i = tid; i < D; i += blockDim.x) outb[i] = 0.f;
         if (tid == 0) {
             ws.tau[bh] = INFINITY;
             if (tau_out) tau_out[bh] = INFINITY;
@@ -711,35 +632,34 @@ tau_kernel(int Hq, int P, float alpha, int cand_cap, WS ws, DecodeLayout L,
         return;
     }
     const float mx = key_float(key);
-    const float* z = ws.z + ((int64_t)u * G + hg) * L.Umax * P;
-    for (int i = tid; i < L.nbw; i += blockDim.x) s_bits[i] = 0u;
 
-    // candidates x = z' - max > -1 (all others have zero weight).  Each tile
-    // is read with coalesced 16-byte loads, all in flight at once, and
-    // compacted in a fixed thread order (deterministic sums below).
-    constexpr int kVec = 8;                                // float4 per thread per tile
-    constexpr int kTile = kTauThreads * kVec * 4;
+    // candidates x = z' - max > -1, compacted in a fixed thread order
     int m = 0;
-    for (int t0 = 0; t0 < n; t0 += kTile) {
-        float v[kVec * 4];
+    for (int t0 = 0; t0 < n; t0 += kTpvTile) {
+        if (t0 > 0) {
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const int i = t0 + (j * kTauThreads + tid) * 4;   // n is a multiple of 4
-            const float4 f = i < n ? __ldcg(reinterpret_cast<const float4*>(z + i))
-                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            v[4 * j] = f.x - mx; v[4 * j + 1] = f.y - mx; v[4 * j + 2] = f.z - mx; v[4 * j + 3] = f.w - mx;
+            for (int j = 0; j < kTpvVec; ++j) {
+                const int i = t0 + (j * kTpvThreads + tid) * 4;
+                const float4 f = i < n ? __ldcg(reinterpret_cast<const float4*>(z + i))
+                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+            }
         }
         int c = 0;
 #pragma unroll
-        for (int j = 0; j < kVec * 4; ++j) c += v[j] > -1.f;
+        for (int j = 0; j < kTpvVec * 4; ++j) {
+            const int i = t0 + ((j >> 2) * kTpvThreads + tid) * 4 + (j & 3);
+            v[j] = i < n ? v[j] - mx : -INFINITY;
+            c += v[j] > -1.f;
+        }
         int tot;
         int pos = m + block_exclusive_scan(c, ired, &tot);
 #pragma unroll
-        for (int j = 0; j < kVec * 4; ++j) {
+        for (int j = 0; j < kTpvVec * 4; ++j) {
             if (v[j] > -1.f) {
                 if (pos < cand_cap) {
                     s_x[pos] = v[j];
-                    s_pos[pos] = t0 + ((j >> 2) * kTauThreads + tid) * 4 + (j & 3);
+                    s_pos[pos] = t0 + ((j >> 2) * kTpvThreads + tid) * 4 + (j & 3);
                 }
                 ++pos;
             }
@@ -749,25 +669,41 @@ tau_kernel(int Hq, int P, float alpha, int cand_cap, WS ws, DecodeLayout L,
     m = min(m, cand_cap);
     __syncthreads();
 
+    // threshold t (relative to the max): f(t) = sum (x - t)_+^e - 1 = 0
     float t;
-    if (E == 0) {
-        const float ex = 1.f / (alpha - 1.f);
-        float lo = -1.f, hi = -powf(static_cast<float>(m), 1.f - alpha);
-        for (int it = 0; it < 48; ++it) {
-            const float mid = 0.5f * (lo + hi);
-            float f = 0.f;
-            for (int i = tid; i < m; i += blockDim.x) {
-                const float a = s_x[i] - mid;
-                if (a > 0.f) f += powf(a, ex);
+    if (E != 0 && m <= 1024) {
+        // one warp, candidates in registers, shuffle-only reductions
+        if (wid == 0) {
+            float xr[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int i = j * 32 + lane;
+                xr[j] = i < m ? s_x[i] : -INFINITY;
             }
-            f = block_sum(f, fred) - 1.f;
-            if (f >= 0.f) lo = mid; else hi = mid;
+            float tt = -1.f;
+            for (int it = 0; it < 64; ++it) {
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float a = xr[j] - tt;
+                    if (a > 0.f) {
+                        if (E == 2) { s0 = fmaf(a, a, s0); s1 += a; }
+                        else { s0 += a; s1 += 1.f; }
+                    }
+                }
+                s0 = warp_sum(s0);
+                s1 = warp_sum(s1);
+                const float dv = E == 2 ? 2.f * s1 : s1;
+                if (!(dv > 0.f)) break;
+                const float step = (s0 - 1.f) / dv;
+                tt += step;
+                if (!(step > 1e-7f)) break;     // at the root to fp32 resolution
+            }
+            if (lane == 0) s_t = tt;
         }
-        t = 0.5f * (lo + hi);
-    } else {
-        // Newton on f(t) = sum (x - t)_+^e - 1 from t = -1 (f >= 0 there: the
-        // maximum alone contributes 1); f is convex and decreasing, so the
-        // iterates increase monotonically to the root.
+        __syncthreads();
+        t = s_t;
+    } else if (E != 0) {
         t = -1.f;
         for (int it = 0; it < 64; ++it) {
             float2 acc = make_float2(0.f, 0.f);
@@ -783,21 +719,69 @@ tau_kernel(int Hq, int P, float alpha, int cand_cap, WS ws, DecodeLayout L,
             if (!(dv > 0.f)) break;
             const float step = (acc.x - 1.f) / dv;
             t += step;
-            if (!(step > 1e-7f)) break;     // at the root to fp32 resolution
+            if (!(step > 1e-7f)) break;
         }
+    } else {
+        const float ex = 1.f / (alpha - 1.f);
+        float lo = -1.f, hi = -powf(static_cast<float>(m), 1.f - alpha);
+        for (int it = 0; it < 48; ++it) {
+            const float mid = 0.5f * (lo + hi);
+            float f = 0.f;
+            for (int i = tid; i < m; i += blockDim.x) {
+                const float a = s_x[i] - mid;
+                if (a > 0.f) f += powf(a, ex);
+            }
+            f = block_sum(f, fred) - 1.f;
+            if (f >= 0.f) lo = mid; else hi = mid;
+        }
+        t = 0.5f * (lo + hi);
     }
-    // support and the pages holding it
+
+    // weights in place; the support's V rows (one round trip for the blocks)
+    const float ex = 1.f / (alpha - 1.f);
+    const T* vbase = static_cast<const T*>(kv.v);
     int sup = 0;
+    float wsum = 0.f;
     for (int i = tid; i < m; i += blockDim.x) {
-        if (s_x[i] > t) {
+        const float a = s_x[i] - t;
+        const float w = a > 0.f ? pow_e(a, E, ex) : 0.f;
+        s_x[i] = w;
+        if (w > 0.f) {
             ++sup;
-            const int page = s_pos[i] / P;
-            atomicOr(&s_bits[page >> 5], 1u << (page & 31));
+            wsum += w;
+            const int pos = s_pos[i];
+            const int ui = pos / P;
+            const int blk = __ldcg(ws.union_blk + (int64_t)u * L.Umax + ui);
+            s_pos[i] = blk >= 0 ? ((blk * Hkv + kvh) * P + (pos - ui * P)) : -1;
+            atomicOr(&ws.vtok[(int64_t)u * L.nvw + (pos >> 5)], 1u << (pos & 31));
         }
     }
     sup = block_sum_i(sup, ired);
-    for (int i = tid; i < L.nbw; i += blockDim.x)
-        if (s_bits[i]) atomicOr(&ws.supp[(int64_t)u * L.nbw + i], s_bits[i]);
+    wsum = block_sum(wsum, fred);      // includes a barrier: weights and rows are visible
+
+    const int lr = tid % LPR;
+    const int rg = tid / LPR;
+    float acc[EPC];
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
+    for (int i = rg; i < m; i += RG) {
+        const float w = s_x[i];
+        const int row = s_pos[i];
+        if (w > 0.f && row >= 0) {
+            float x[EPC];
+            Elem<T>::widen(ld_nc_v4(vbase + (int64_t)row * D + lr * EPC), x);
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) s_red[rg * D + lr * EPC + e] = acc[e];
+    __syncthreads();
+    for (int d = tid; d < D; d += blockDim.x) {
+        float o = 0.f;
+        for (int r = 0; r < RG; ++r) o += s_red[r * D + d];
+        outb[d] = wsum > 0.f ? o / wsum : 0.f;
+    }
     if (tid == 0) {
         const float tau = t + mx;
         ws.tau[bh] = tau;
@@ -806,231 +790,29 @@ tau_kernel(int Hq, int P, float alpha, int cand_cap, WS ws, DecodeLayout L,
     }
 }
 
-// ---------------------------------------------------------------------------
-// pv: weights and value accumulation over the support pages, merge
-// ---------------------------------------------------------------------------
-// Persistent: a work item is (unit, chunk of up to chv support pages); a unit
-// with no support page gets one item that writes zeros.  CTA i takes items
-// i, i + gridDim.x, ...
-template <typename T, int D, int G, int E>
-__global__ void __launch_bounds__(kPvThreads)
-pv_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __restrict__ out, int chv) {
-    constexpr int EPC = Elem<T>::kPer16;
-    constexpr int LPR = D / EPC;              // lanes per value row
-    constexpr int RG = kPvThreads / LPR;      // row groups
-    constexpr int NWP = kPvThreads / 32;
-    extern __shared__ __align__(128) unsigned char s_raw[];
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ int s_act[kPvMaxChunk], s_blk[kPvMaxChunk];
-    __shared__ int red[40];
-    __shared__ float s_tau[G], s_psum[G];
-    __shared__ float s_wps[NWP][G];
-    __shared__ int s_last;
-
-    const int P = kv.P;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const size_t page_elems = (size_t)P * D;
-    const uint32_t page_bytes = (uint32_t)(page_elems * sizeof(T));
-    const size_t vbytes = (size_t)chv * page_bytes, rbytes = (size_t)RG * G * D * sizeof(float);
-    const size_t stage_bytes = vbytes > rbytes ? vbytes : rbytes;
-    // shared layout: V pages (later the reduction buffer) | weights [chv][P][G]
-    // | support pages per unit [U] | first work item per unit [U + 1]
-    T* stage = reinterpret_cast<T*>(s_raw);
-    float* s_red = reinterpret_cast<float*>(s_raw);
-    float* s_w = reinterpret_cast<float*>(s_raw + stage_bytes);
-    int* s_nact = reinterpret_cast<int*>(s_w + (size_t)chv * P * G);
-    int* s_start = s_nact + L.U;
-
-    for (int i = tid; i < L.U; i += blockDim.x) s_nact[i] = 0;
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
-    }
+__global__ void count_rows_kernel(WS ws, DecodeLayout L) {
+    const int u = blockIdx.x;
+    int c = 0;
+    for (int i = threadIdx.x; i < L.nvw; i += blockDim.x) c += __popc(ws.vtok[(int64_t)u * L.nvw + i]);
+    c = warp_sum_i(c);
+    __shared__ int part[32];
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
     __syncthreads();
-    for (int i = tid; i < L.U * L.nbw; i += blockDim.x) {
-        const int c = __popc(ws.supp[i]);
-        if (c) atomicAdd(&s_nact[i / L.nbw], c);
-    }
-    __syncthreads();
-    {
-        const int seg = (L.U + blockDim.x - 1) / blockDim.x;
-        const int a0 = min(L.U, tid * seg), a1 = min(L.U, a0 + seg);
-        int c = 0;
-        for (int a = a0; a < a1; ++a) c += max(1, (s_nact[a] + chv - 1) / chv);
-        int tot;
-        int run = block_exclusive_scan(c, red, &tot);
-        for (int a = a0; a < a1; ++a) {
-            s_start[a] = run;
-            run += max(1, (s_nact[a] + chv - 1) / chv);
-        }
-        if (tid == 0) s_start[L.U] = tot;
-    }
-    __syncthreads();
-    const int items = s_start[L.U];
-    const float ex = 1.f / (alpha - 1.f);
-    const T* vbase = static_cast<const T*>(kv.v);
-    uint32_t phase = 0;
-
-    for (int item = blockIdx.x; item < items; item += gridDim.x) {
-        int lo = 0, hi = L.U - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_start[mid] <= item) lo = mid; else hi = mid - 1;
-        }
-        const int u = lo;
-        const int c = item - s_start[u];
-        const int nact = s_nact[u];
-        const int b = u / kv.hkv;
-        const int kvh = u - b * kv.hkv;
-        float* outb = out + ((int64_t)b * Hq + kvh * G) * D;
-        if (nact == 0) {            // uniform across the CTA
-            for (int i = tid; i < G * D; i += blockDim.x) outb[i] = 0.f;
-            if (tid == 0) ws.vpages[u] = 0;
-            continue;
-        }
-        const int nchunks = (nact + chv - 1) / chv;
-        const int a0 = c * chv;
-        const int npg = min(nact, a0 + chv) - a0;
-        {
-            // this chunk's support pages, in union order (nbw <= kPvThreads)
-            const uint32_t word = tid < L.nbw ? ws.supp[(int64_t)u * L.nbw + tid] : 0u;
-            int all;
-            int r = block_exclusive_scan(__popc(word), red, &all);
-            uint32_t w = word;
-            while (w && r < a0 + chv) {
-                const int bit = __ffs(w) - 1;
-                w &= w - 1;
-                if (r >= a0) s_act[r - a0] = tid * 32 + bit;
-                ++r;
-            }
-        }
-        if (tid < G) s_tau[tid] = ws.tau[b * Hq + kvh * G + tid];
-        if (tid == 0 && c == 0) ws.vpages[u] = nact;
-        __syncthreads();
-        if (tid < npg) {
-            const int page = ws.union_page[(int64_t)u * L.Umax + s_act[tid]];
-            const int blk = kv.pt[(int64_t)b * kv.maxp + page];
-            s_blk[tid] = (blk < 0 || blk >= kv.nb) ? -1 : blk;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            uint32_t bytes = 0;
-            for (int j = 0; j < npg; ++j) bytes += s_blk[j] >= 0 ? page_bytes : 0u;
-            mbar_arrive_expect_tx(&bar, bytes);
-            for (int j = 0; j < npg; ++j)
-                if (s_blk[j] >= 0)
-                    bulk_g2s(stage + (size_t)j * page_elems,
-                             vbase + ((int64_t)s_blk[j] * kv.hkv + kvh) * page_elems, page_bytes, &bar);
-        }
-
-        // weights, while the copies are in flight
-        float ps[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) ps[h] = 0.f;
-        for (int idx = tid; idx < npg * P; idx += blockDim.x) {
-            const int j = idx / P, t = idx - j * P;
-            const int i = s_act[j];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float a = __ldcg(ws.z + (((int64_t)u * G + h) * L.Umax + i) * P + t) - s_tau[h];
-                const float w = a > 0.f ? pow_e(a, E, ex) : 0.f;
-                s_w[idx * G + h] = w;
-                ps[h] += w;
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float v = warp_sum(ps[h]);
-            if (lane == 0) s_wps[wid][h] = v;
-        }
-        const bool ok = __syncthreads_and(mbar_wait(&bar, phase));
-        phase ^= 1u;
-        if (!ok) {
-            if (tid == 0) flag_bad_data();
-            return;
-        }
-        if (tid < G) {
-            float sum = 0.f;
-            for (int w = 0; w < NWP; ++w) sum += s_wps[w][tid];
-            s_psum[tid] = sum;
-        }
-
-        const int lr = tid % LPR;
-        const int rg = tid / LPR;
-        float acc[G][EPC];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) acc[h][e] = 0.f;
-        for (int r = rg; r < npg * P; r += RG) {
-            float w[G];
-            bool any = false;
-#pragma unroll
-            for (int h = 0; h < G; ++h) { w[h] = s_w[r * G + h]; any |= w[h] > 0.f; }
-            if (!any) continue;
-            float x[EPC];
-            Elem<T>::widen(*reinterpret_cast<const uint4*>(stage + (size_t)r * D + lr * EPC), x);
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < EPC; ++e) acc[h][e] = fmaf(w[h], x[e], acc[h][e]);
-        }
-        __syncthreads();   // the stage area becomes the reduction buffer
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) s_red[((size_t)rg * G + h) * D + lr * EPC + e] = acc[h][e];
-        __syncthreads();
-        if (nchunks == 1) {
-            for (int i = tid; i < G * D; i += blockDim.x) {
-                float so = 0.f;
-                for (int g = 0; g < RG; ++g) so += s_red[(size_t)g * G * D + i];
-                const float sp = s_psum[i / D];
-                outb[i] = sp > 0.f ? so / sp : 0.f;
-            }
-        } else {
-            float* part = ws.partial + ((int64_t)u * L.SmaxV + c) * G * (D + 1);
-            for (int i = tid; i < G * D; i += blockDim.x) {
-                float so = 0.f;
-                for (int g = 0; g < RG; ++g) so += s_red[(size_t)g * G * D + i];
-                part[i] = so;
-            }
-            if (tid < G) part[G * D + tid] = s_psum[tid];
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) s_last = atomicAdd(&ws.counter[u], 1) == nchunks - 1;
-            __syncthreads();
-            if (s_last) {
-                __threadfence();
-                const float* part0 = ws.partial + (int64_t)u * L.SmaxV * G * (D + 1);
-                for (int i = tid; i < G * D; i += blockDim.x) {
-                    const int h = i / D;
-                    float so = 0.f, sp = 0.f;
-                    for (int cc = 0; cc < nchunks; ++cc) {
-                        const float* pc = part0 + (int64_t)cc * G * (D + 1);
-                        so += __ldcg(pc + i);
-                        sp += __ldcg(pc + G * D + h);
-                    }
-                    outb[i] = sp > 0.f ? so / sp : 0.f;
-                }
-                if (tid == 0) ws.counter[u] = 0;
-            }
-        }
-        // the next item's bulk copies overwrite the reduction buffer: order
-        // this thread's shared-memory writes before those async-proxy writes
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
+    if (threadIdx.x == 0) {
+        int s = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += part[w];
+        ws.vrows[u] = s;
     }
 }
 
 // ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
-static cudaEvent_t g_stage_events[5];
+static cudaEvent_t g_stage_events[4];
 static int g_n_stage_events = 0;
 
 void set_decode_stage_events(const cudaEvent_t* events, int n) {
-    g_n_stage_events = (events && n == 5) ? 5 : 0;
+    g_n_stage_events = (events && n == 4) ? 4 : 0;
     for (int i = 0; i < g_n_stage_events; ++i) g_stage_events[i] = events[i];
 }
 
@@ -1045,15 +827,19 @@ static void stage_mark(int i, cudaStream_t s) {
         cudaEventRecord(g_stage_events[i], s);
 }
 
-cudaError_t read_decode_counts(const void* ws_base, const DecodeLayout& L, int32_t* union_pages,
-                               int32_t* v_pages, cudaStream_t s) {
-    const char* c = static_cast<const char*>(ws_base);
+cudaError_t read_decode_counts(void* ws_base, const DecodeLayout& L, int32_t* union_pages,
+                               int32_t* v_rows, cudaStream_t s) {
+    const WS ws = ws_views(ws_base, L);
     cudaError_t e = cudaSuccess;
     if (union_pages)
-        e = cudaMemcpyAsync(union_pages, c + L.union_count, sizeof(int32_t) * L.U,
+        e = cudaMemcpyAsync(union_pages, ws.union_count, sizeof(int32_t) * L.U,
                             cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess && v_pages)
-        e = cudaMemcpyAsync(v_pages, c + L.vpages, sizeof(int32_t) * L.U, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && v_rows) {
+        count_rows_kernel<<<L.U, 256, 0, s>>>(ws, L);
+        e = cudaGetLastError();
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(v_rows, ws.vrows, sizeof(int32_t) * L.U, cudaMemcpyDeviceToHost, s);
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return e;
 }
@@ -1069,35 +855,21 @@ static int sm_count() {
     return v;
 }
 
-template <int E, typename T, int D, int G>
-static cudaError_t launch_tau_pv(float alpha, int Hq, const KV& kv, const WS& ws,
-                                 const DecodeLayout& L, int cap, float* out, float* tau_out,
-                                 int32_t* support_out, cudaStream_t s) {
+template <int E, typename T, int D>
+static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
+                              const DecodeLayout& L, int cap, float* out, float* tau_out,
+                              int32_t* support_out, cudaStream_t s) {
+    constexpr int RG = kTpvThreads / (D / Elem<T>::kPer16);
     const int cand_cap = cap * kv.P;
-    const size_t tsmem = (size_t)cand_cap * 8 + (size_t)L.nbw * 4;
-    cudaError_t e = cudaFuncSetAttribute(tau_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tsmem);
+    const size_t smem = (size_t)cand_cap * 8 + (size_t)RG * D * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(tpv_kernel<T, D, E>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     stage_mark(2, s);
-    tau_kernel<E><<<kv.B * Hq, kTauThreads, tsmem, s>>>(Hq, kv.P, alpha, cand_cap, ws, L, tau_out,
-                                                         support_out);
+    tpv_kernel<T, D, E><<<kv.B * Hq, kTpvThreads, smem, s>>>(Hq, alpha, cand_cap, kv, ws, L, out,
+                                                             tau_out, support_out);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-    constexpr int EPC = Elem<T>::kPer16;
-    constexpr int RG = kPvThreads / (D / EPC);
-    const size_t page_bytes = (size_t)kv.P * D * sizeof(T);
-    const int chv = (int)std::max<size_t>(L.CHV, std::min<size_t>(kPvMaxChunk, kPvStageBytes / page_bytes));
-    const size_t stage_bytes = std::max((size_t)chv * page_bytes, (size_t)RG * G * D * sizeof(float));
-    const size_t psmem = stage_bytes + (size_t)chv * kv.P * G * sizeof(float) +
-                         (size_t)(2 * L.U + 1) * sizeof(int);
-    e = cudaFuncSetAttribute(pv_kernel<T, D, G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)psmem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid(sm_count());
     stage_mark(3, s);
-    pv_kernel<T, D, G, E><<<grid, kPvThreads, psmem, s>>>(Hq, alpha, kv, ws, L, out, chv);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    stage_mark(4, s);
     return cudaSuccess;
 }
 
@@ -1107,13 +879,12 @@ static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV
                                    float* out, float* tau_out, int32_t* support_out, const WS& ws,
                                    const DecodeLayout& L, cudaStream_t s) {
     cudaError_t e;
-    if (L.U > kMaxUnits || L.nbw > kPvThreads) return cudaErrorInvalidValue;
+    if (L.U > kMaxUnits || cap > kPlanSelRegs * kPlanThreads / G) return cudaErrorInvalidValue;
+    stage_mark(0, s);
     {
-        const int nwm = (kv.maxp + 31) / 32;
-        const size_t smem = (size_t)G * nwm * 4;
+        const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax);
         e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        stage_mark(0, s);
         plan_kernel<G><<<L.U, kPlanThreads, smem, s>>>(kv, Hq, sel, n_sel, cap, ws, L);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -1144,9 +915,9 @@ static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const int E = fabsf(alpha - 1.5f) < 1e-6f ? 2 : (fabsf(alpha - 2.f) < 1e-6f ? 1 : 0);
-    if (E == 2) return launch_tau_pv<2, T, D, G>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
-    if (E == 1) return launch_tau_pv<1, T, D, G>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
-    return launch_tau_pv<0, T, D, G>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
+    if (E == 2) return launch_tpv<2, T, D>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
+    if (E == 1) return launch_tpv<1, T, D>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
+    return launch_tpv<0, T, D>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
 }
 
 cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, const int32_t* sel,

@@ -26,13 +26,13 @@ struct KV {
 // Workspace of one decode call, carved from the caller's buffer.  U = B * Hkv
 // units (sequence, kv head); a unit reads the union of its G heads' selected
 // pages (at most Umax of them) once.  Scores are kept per unit in union order,
-// [U][G][Umax * P], with -inf where a head did not select the page.  The value
-// stage reads only union pages holding a positive weight (a bitmap of nbw words
-// per unit), CHV of them per CTA, at most SmaxV CTAs per unit.
+// [U][G][Umax * P], with -inf where a head did not select the page; the
+// physical block of every union page is kept for the value stage.  vtok marks,
+// per unit, the tokens whose V row was read (nvw words per unit).
 struct DecodeLayout {
-    int    U, G, Umax, nbw, CHV, SmaxV;
-    size_t union_count, counter, vpages, head_max, union_page, union_mask, supp;
-    size_t z, tau, partial, total;
+    int    U, G, Umax, nvw;
+    size_t union_count, head_max, union_page, union_mask, union_blk, vtok, vrows;
+    size_t z, tau, total;
 };
 DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap);
 
@@ -51,15 +51,15 @@ cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, con
                           const int32_t* n_sel, int cap, float alpha, float* out, float* tau_out,
                           int32_t* support_out, void* ws, const DecodeLayout& L, cudaStream_t s);
 
-// Optional events recorded between the decode kernels (plan | qk | tau | pv):
-// events[0] before plan, [1] before qk, [2] before tau, [3] before pv,
-// [4] after pv.  n = 0 disables.  Process-wide; for measurement only.
+// Optional events recorded between the decode kernels (plan | qk | tpv):
+// events[0] before plan, [1] before qk, [2] before tpv, [3] after tpv.
+// n = 0 disables.  Process-wide; for measurement only.
 void set_decode_stage_events(const cudaEvent_t* events, int n);
 
 // Per-unit counters of the last decode that used this workspace: union pages
-// whose K was read, and pages whose V was read.
-cudaError_t read_decode_counts(const void* ws, const DecodeLayout& L, int32_t* union_pages,
-                               int32_t* v_pages, cudaStream_t s);
+// whose K was read, and distinct tokens whose V row was read.
+cudaError_t read_decode_counts(void* ws, const DecodeLayout& L, int32_t* union_pages,
+                               int32_t* v_rows, cudaStream_t s);
 
 // Sticky device-data check words, one per translation unit: read, OR'd into
 // *flag, and cleared.

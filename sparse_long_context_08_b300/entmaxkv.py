@@ -288,7 +288,7 @@ def entmaxkv_read_device_status(stream=None) -> int:
 
 
 def entmaxkv_set_stage_events(events: list | None) -> None:
-    """events: five torch.cuda.Event(enable_timing=True), or None to disable."""
+    """events: four torch.cuda.Event(enable_timing=True), or None to disable."""
     if not events:
         _check("entmaxkv_set_stage_events", lib().entmaxkv_set_stage_events(None, 0))
         return
@@ -301,7 +301,8 @@ def entmaxkv_set_stage_events(events: list | None) -> None:
 
 def entmaxkv_decode_counts(workspace: torch.Tensor, batch, num_q_heads, num_kv_heads, head_dim,
                            page_size, max_pages, cap_pages, stream=None):
-    """Per-unit (union pages read for K, pages read for V) of the last decode."""
+    """Per-unit (union pages read for K, distinct tokens whose V row was read)
+    of the last decode."""
     import numpy as np
     U = batch * num_kv_heads
     up = np.zeros(U, np.int32)

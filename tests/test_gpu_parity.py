@@ -231,3 +231,4 @@ def test_graph_capture_replays_the_step():
     torch.cuda.synchronize()
     out = g.dec.out.cpu().numpy().astype(np.float64).reshape(ref["out"].shape)
     assert np.array_equal(out, ref["out"])
+

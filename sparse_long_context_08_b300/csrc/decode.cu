@@ -75,6 +75,7 @@ template <int G>
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(KV kv, int Hq, const int32_t* __restrict__ sel, const int32_t* __restrict__ n_sel,
             int cap, WS ws, DecodeLayout L) {
+    pdl_enter();
     extern __shared__ __align__(16) uint32_t s_plan[];   // bitmaps, then union pages
     __shared__ int red[40];
     __shared__ int s_ns[G];
@@ -132,6 +133,7 @@ template <typename T, int D, int G>
 __global__ void __launch_bounds__(kQkThreads, 1)
 qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, DecodeLayout L,
           int nslots, int group) {
+    pdl_enter();
     using C = QkCfg<T, D, G>;
     extern __shared__ __align__(128) unsigned char s_raw[];
     __shared__ int red[40];
@@ -392,6 +394,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kQmWarps * 32, kQmCtasPerSm)
 qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, DecodeLayout L,
               int ns) {
+    pdl_enter();
     using C = QmCfg<D, G>;
     extern __shared__ __align__(128) unsigned char s_qm[];
     __shared__ int red[40];
@@ -585,6 +588,7 @@ template <typename T, int D, int E>   // E: 2 alpha = 1.5, 1 alpha = 2, 0 any ot
 __global__ void __launch_bounds__(kTpvThreads)
 tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
            float* __restrict__ out, float* __restrict__ tau_out, int32_t* __restrict__ support_out) {
+    pdl_enter();
     constexpr int EPC = Elem<T>::kPer16;
     constexpr int LPR = D / EPC;              // lanes per V row
     constexpr int RG = kTpvThreads / LPR;     // V rows per pass
@@ -866,9 +870,9 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     stage_mark(2, s);
-    tpv_kernel<T, D, E><<<kv.B * Hq, kTpvThreads, smem, s>>>(Hq, alpha, cand_cap, kv, ws, L, out,
-                                                             tau_out, support_out);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_pdl(tpv_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvThreads), smem, s, Hq, alpha,
+                   cand_cap, kv, ws, L, out, tau_out, support_out);
+    if (e != cudaSuccess) return e;
     stage_mark(3, s);
     return cudaSuccess;
 }
@@ -885,8 +889,9 @@ static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV
         const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax);
         e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        plan_kernel<G><<<L.U, kPlanThreads, smem, s>>>(kv, Hq, sel, n_sel, cap, ws, L);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel,
+                       cap, ws, L);
+        if (e != cudaSuccess) return e;
     }
     if constexpr (sizeof(T) == 2) {
         const int page_bytes = kv.P * D * 2;
@@ -896,9 +901,9 @@ static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV
         e = cudaFuncSetAttribute(qk_mma_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
-        qk_mma_kernel<D, G><<<sm_count() * kQmCtasPerSm, kQmWarps * 32, smem, s>>>(
-            q, Hq, (alpha - 1.f) * scale, kv, ws, L, ns);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(qk_mma_kernel<D, G>, dim3(sm_count() * kQmCtasPerSm), dim3(kQmWarps * 32),
+                       smem, s, q, Hq, (alpha - 1.f) * scale, kv, ws, L, ns);
+        if (e != cudaSuccess) return e;
     } else {
         const size_t page_bytes = (size_t)kv.P * D * sizeof(T);
         const size_t fixed = (size_t)kQkConsumers * G * kv.P * 4 + (size_t)((L.U + 1 + 3) & ~3) * 4;
@@ -910,9 +915,9 @@ static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV
         e = cudaFuncSetAttribute(qk_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
-        qk_kernel<T, D, G><<<sm_count(), kQkThreads, smem, s>>>(q, Hq, (alpha - 1.f) * scale, kv, ws, L,
-                                                               ns, std::min(kQkGroup, ns));
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(qk_kernel<T, D, G>, dim3(sm_count()), dim3(kQkThreads), smem, s, q, Hq,
+                       (alpha - 1.f) * scale, kv, ws, L, ns, std::min(kQkGroup, ns));
+        if (e != cudaSuccess) return e;
     }
     const int E = fabsf(alpha - 1.5f) < 1e-6f ? 2 : (fabsf(alpha - 2.f) < 1e-6f ? 1 : 0);
     if (E == 2) return launch_tpv<2, T, D>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);

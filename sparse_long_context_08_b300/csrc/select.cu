@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kTopkMaxThreads)
 select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
                    int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
                    float* __restrict__ aux) {
+    pdl_enter();
     extern __shared__ __align__(16) uint32_t keys[];   // [max_pages]
     __shared__ int hist[256];
     __shared__ uint32_t umin_red[32], umax_red[32];
@@ -295,6 +296,7 @@ __global__ void __launch_bounds__(kSelThreads)
 select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float alpha,
                     float delta, int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
                     float* __restrict__ aux) {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ SelShared sh;
     __shared__ float2 fred[32];
@@ -412,8 +414,8 @@ cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp,
     cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    select_topk_kernel<<<kv.B * Hq, threads, smem, s>>>(bound, kv, Hq, kp, sel, n_sel, aux);
-    return cudaGetLastError();
+    return launch_pdl(select_topk_kernel, dim3(kv.B * Hq), dim3(threads), smem, s, bound, kv, Hq,
+                      kp, sel, n_sel, aux);
 }
 
 cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, float alpha,
@@ -428,14 +430,16 @@ cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, 
         e = cudaFuncSetAttribute(select_gauss_kernel<2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        select_gauss_kernel<2><<<kv.B * Hq, threads, smem, s>>>(ms, kv, Hq, cap, alpha, delta,
-                                                                 sel, n_sel, aux);
+        e = launch_pdl(select_gauss_kernel<2>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
+                       Hq, cap, alpha, delta, sel, n_sel, aux);
+        if (e != cudaSuccess) return e;
     } else {
         e = cudaFuncSetAttribute(select_gauss_kernel<1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        select_gauss_kernel<1><<<kv.B * Hq, threads, smem, s>>>(ms, kv, Hq, cap, alpha, delta,
-                                                                 sel, n_sel, aux);
+        e = launch_pdl(select_gauss_kernel<1>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
+                       Hq, cap, alpha, delta, sel, n_sel, aux);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -3,8 +3,8 @@
 // Top-k (§2.B.1): one CTA per (sequence, query head) holds the head's page
 // bounds as order-preserving uint32 keys in shared memory, finds the boundary
 // with an MSB radix select that starts at the highest bit where the keys
-// differ, then writes the selected pages in ascending order with one block
-// scan: ties at the k-th key go to the lower page ids.
+// differ, then writes the selected pages in ascending order, ranked with warp
+// ballots: ties at the k-th key go to the lower page ids.
 //
 // Gaussian tau-hat (§2.B.2): one CTA per (sequence, query head) solves
 //   F(tau) = sum_p n_p E[((alpha-1) X_p - tau)_+^e] - 1 = 0,  X_p ~ N(m_p, s_p^2)
@@ -149,11 +149,23 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
         return;
     }
     uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
-    for (int i = tid; i < np; i += nt) {
-        const uint32_t key = float_key(__ldcg(src + i));
-        keys[i] = key;
-        kmn = min(kmn, key);
-        kmx = max(kmx, key);
+    for (int base = 0; base < np; base += 16 * nt) {
+        float v[16];                       // 16 coalesced loads in flight per thread
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = base + j * nt + tid;
+            v[j] = i < np ? __ldcg(src + i) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = base + j * nt + tid;
+            if (i < np) {
+                const uint32_t key = float_key(v[j]);
+                keys[i] = key;
+                kmn = min(kmn, key);
+                kmx = max(kmx, key);
+            }
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -216,39 +228,48 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     }
     const int takeB = rem;    // == nB when B is taken whole
 
-    // compaction in page order: one packed scan of (above, in-B) counts
-    const int seg = (np + nt - 1) / nt;
-    const int i0 = min(np, tid * seg), i1 = min(np, i0 + seg);
-    int na = 0, nb_ = 0;
-    for (int i = i0; i < i1; ++i) {
-        const uint64_t kh = (uint64_t)keys[i] >> shift;
-        na += kh > hi;
-        nb_ += kh == hi;
+    // compaction in page order: every warp walks a contiguous range of 32-key
+    // chunks (consecutive shared-memory words, no bank conflicts) and ranks
+    // keys with ballots; one prefix over the warp totals places the ranges
+    __shared__ int s_wa[32], s_wb[32];
+    const uint32_t below = (1u << lane) - 1u;
+    const int nch = (np + 31) / 32;
+    const int ch0 = nch * wid / nwarps, ch1 = nch * (wid + 1) / nwarps;
+    int wa = 0, wb = 0;
+    for (int c = ch0; c < ch1; ++c) {
+        const int i = c * 32 + lane;
+        const bool in = i < np;
+        const uint64_t kh = in ? (uint64_t)keys[i] >> shift : 0u;
+        wa += __popc(__ballot_sync(0xFFFFFFFFu, in && kh > hi));
+        wb += __popc(__ballot_sync(0xFFFFFFFFu, in && kh == hi));
     }
-    // both counts are below 2^16 (max_pages <= 49152): the packed sum fits
-    // 32 unsigned bits
-    int tot;
-    const uint32_t ex = static_cast<uint32_t>(block_exclusive_scan((na << 16) | nb_, ired, &tot));
-    int a = static_cast<int>(ex >> 16), r = static_cast<int>(ex & 0xFFFFu);
+    if (lane == 0) { s_wa[wid] = wa; s_wb[wid] = wb; }
+    __syncthreads();
+    int a = 0, r = 0;
+    for (int w = 0; w < wid; ++w) { a += s_wa[w]; r += s_wb[w]; }
     uint32_t tmin = 0xFFFFFFFFu, nmax = 0u;
     bool any_out = false;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t key = keys[i];
+    for (int c = ch0; c < ch1; ++c) {
+        const int i = c * 32 + lane;
+        const bool in = i < np;
+        const uint32_t key = in ? keys[i] : 0u;
         const uint64_t kh = (uint64_t)key >> shift;
+        const uint32_t ma = __ballot_sync(0xFFFFFFFFu, in && kh > hi);
+        const uint32_t mb = __ballot_sync(0xFFFFFFFFu, in && kh == hi);
+        const int ra = a + __popc(ma & below);     // above keys before i
+        const int rb = r + __popc(mb & below);     // boundary-bin keys before i
         bool take = false;
-        if (kh > hi) {
-            dst[a + min(r, takeB)] = i;
-            ++a;
+        if (in && kh > hi) {
+            dst[ra + min(rb, takeB)] = i;
             take = true;
-        } else if (kh == hi) {
-            if (r < takeB) {
-                dst[a + r] = i;
-                take = true;
-            }
-            ++r;
+        } else if (in && kh == hi && rb < takeB) {
+            dst[ra + rb] = i;
+            take = true;
         }
         if (take) tmin = min(tmin, key);
-        else { nmax = max(nmax, key); any_out = true; }
+        else if (in) { nmax = max(nmax, key); any_out = true; }
+        a += __popc(ma);
+        r += __popc(mb);
     }
     // smallest taken key (the k-th bound) and largest key left out
     const int any = __syncthreads_or(any_out);

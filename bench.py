@@ -153,6 +153,25 @@ def bus_id_of(dev: int) -> str | None:
         return None
 
 
+def measured_traffic(workload: str, kernel: str, batch: int):
+    """DRAM bytes (read + write) of one launch of `kernel` from the committed ncu
+    summary, scaled to the launch; None when there is no capture for this
+    workload, or the kernel's source has changed since it was taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            tr = json.load(f)
+        k = tr["kernels"][kernel]
+        if tr.get("workload") != workload or batch != tr.get("batch"):
+            return None
+        with open(os.path.join(ROOT, k["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != k["source_sha256"]:
+                return None
+        return int(k["bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 # ---------------------------------------------------------------------------
 # oracle (CPU) timing: the cpu_baseline leg and the reference arm
 # ---------------------------------------------------------------------------
@@ -333,16 +352,7 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     dom_bytes = per_kernel_bytes.get(dom)
     achieved = dom_bytes / (mean[dom] * 1e-3) / 1e9 if dom_bytes else None
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            with open(tpath) as f:
-                tr = json.load(f)
-            if tr.get("workload") == args.workload and tr.get("kernel") == dom:
-                traffic = tr.get("bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = measured_traffic(args.workload, dom, w.batch)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
                 "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,

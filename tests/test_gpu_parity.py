@@ -112,6 +112,27 @@ def test_gauss_reduced(alpha):
 
 
 # ---------------------------------------------------------------------------
+# the five workloads at their full sizes, through the same decoder and launch
+# shapes the benchmark uses; the oracle checks a seeded sample of query heads
+# (every stage of those heads: bounds, selection, tau, output) and the page
+# metadata of every block
+# ---------------------------------------------------------------------------
+
+def sampled_heads(w, n, seed=11):
+    BH = w.batch * w.num_q_heads
+    rng = np.random.default_rng(seed)
+    return sorted(rng.choice(BH, size=min(n, BH), replace=False).tolist())
+
+
+@pytest.mark.parametrize("name,alpha", [("tiny", 1.5), ("gqa32k", 1.5), ("long128k", 1.5),
+                                        ("long128k", 2.0), ("ctx1m", 1.5), ("gauss64k", 1.5)])
+def test_full_size_sampled_heads(name, alpha):
+    w = make_workload(name, alpha=alpha)
+    full_parity(w, heads=sampled_heads(w, 64))
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
 # shapes: head_dim, dtype, group size, page size, general alpha
 # ---------------------------------------------------------------------------
 

@@ -3,6 +3,7 @@
 // copy (TMA, cp.async.bulk) primitives used to stage K/V pages.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -304,9 +305,32 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
         " [%0], [%1], %2, [%3], %4;"
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
 }
-__device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-                 ::"r"(smem_u32(dst)), "l"(src), "l"(policy) : "memory");
+
+// ---------------------------------------------------------------------------
+// exact bf16 splitting and the bf16 tensor-core product
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t bf16_rn_bits(float x) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+}
+
+// Term s (0 hi, 1 mid, 2 lo) of the three-way bf16 split of x: hi + mid + lo
+// == x exactly for normal x (8 + 8 + 8 significand bits cover fp32's 24).
+__device__ __forceinline__ uint32_t split_term(float x, int s) {
+    const uint32_t hi = bf16_rn_bits(x);
+    const float r1 = x - __uint_as_float(hi << 16);
+    const uint32_t mid = bf16_rn_bits(r1);
+    const float r2 = r1 - __uint_as_float(mid << 16);
+    const uint32_t lo = bf16_rn_bits(r2);
+    return s == 0 ? hi : (s == 1 ? mid : lo);
+}
+
+// c += A (16 x 16, row) * B (16 x 8, col), bf16 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 }  // namespace ekv

@@ -339,28 +339,6 @@ struct QmCfg {
     static constexpr int KS = D / 16;             // k-steps
 };
 
-__device__ __forceinline__ uint32_t bf16_rn_bits(float x) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
-}
-
-// Term s (0 hi, 1 mid, 2 lo) of the exact three-way bf16 split of x.
-__device__ __forceinline__ uint32_t split_term(float x, int s) {
-    const uint32_t hi = bf16_rn_bits(x);
-    const float r1 = x - __uint_as_float(hi << 16);
-    const uint32_t mid = bf16_rn_bits(r1);
-    const float r2 = r1 - __uint_as_float(mid << 16);
-    const uint32_t lo = bf16_rn_bits(r2);
-    return s == 0 ? hi : (s == 1 ? mid : lo);
-}
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 struct PgDesc { int blk, u, i, valid, mask; };
 
 __device__ __forceinline__ PgDesc resolve_page(int f, int f1, const int* prefix, const KV& kv,

@@ -30,6 +30,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "sparse entmax decode µs/step and achieved HBM GB/s (frac of peak) at 128K ctx"
+FULL_METRIC = "full-cache entmax decode µs/step and achieved HBM GB/s (frac of peak)"
 FALLBACK_HBM_GBS = 6400.0
 KERNELS_PER_STEP = 5   # score, select, plan, qk, tpv (threshold + values)
 
@@ -49,6 +50,8 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--mode", choices=["sparse", "full"], default="sparse",
+                    help="sparse: the EntmaxKV step (headline); full: full-cache entmax decode")
     return ap.parse_args()
 
 
@@ -208,6 +211,31 @@ def oracle_time_per_step(w, seconds: float, steps: int | None = None):
     return statistics.mean(times), desc, cores, times
 
 
+def oracle_full_time_per_step(w, seconds: float, steps: int = 1):
+    """Times the fp64 oracle's full-cache entmax attention on a bounded sample
+    of query heads; returns (us per full step, sample description, cores)."""
+    import numpy as np
+    import oracle
+    kv = oracle.KV(w)
+    BH = w.batch * w.num_q_heads
+    cores = oracle.get_threads()
+    n0 = min(BH, cores)
+    t0 = time.perf_counter()
+    oracle.decode_full(kv, float(w.scale), w.alpha, heads=np.arange(n0, dtype=np.int32))
+    per_head = max(1e-6, (time.perf_counter() - t0) / n0)        # wall time per head, parallel
+    n_heads = int(min(BH, max(n0, seconds / max(1, steps) / per_head)))
+    rng = np.random.default_rng(0)
+    times = []
+    for _ in range(steps):
+        heads = np.sort(rng.choice(BH, size=n_heads, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.decode_full(kv, float(w.scale), w.alpha, heads=heads)
+        times.append((time.perf_counter() - t0) * 1e6 * BH / n_heads)
+    desc = (f"{n_heads} of {BH} query heads per step (full-cache scores, exact tau, attention; "
+            f"fp64), {steps} steps, scaled to a full step")
+    return statistics.mean(times), desc, cores
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -215,6 +243,21 @@ def run_reference(args):
     from sparse_long_context_08_b300.workloads import make_workload
     w = make_workload(args.workload, **overrides(args))
     budget = 150.0
+    if args.mode == "full":
+        oracle_full_time_per_step(w, budget * 0.1, steps=max(1, min(args.warmup, 3)))
+        us, desc, cores = oracle_full_time_per_step(w, budget, steps=max(1, min(args.steps, 5)))
+        line = {"metric": FULL_METRIC, "impl": "reference", "value": us, "unit": "us/step",
+                "n_gpus": args.gpus, "steps": max(1, min(args.steps, 5)), "warmup": args.warmup,
+                "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": dict(workload_config(w), mode="full-cache"),
+                "cpu_baseline": {"value": us, "unit": "us/step", "cores": cores,
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line), flush=True)
+        return
     oracle_time_per_step(w, budget * 0.1, steps=max(1, args.warmup))   # warm-up steps
     us, desc, cores, _ = oracle_time_per_step(w, budget, steps=args.steps)
     line = {"metric": METRIC, "impl": "reference", "value": us, "unit": "us/step",
@@ -416,10 +459,169 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_full(args):
+    """Full-cache entmax decode (every valid token): plan -> qk -> tpv over the
+    whole cache, timed like the sparse step."""
+    import torch
+    import torch.distributed as dist
+
+    from sparse_long_context_08_b300 import entmaxkv as E
+    from sparse_long_context_08_b300.api import EntmaxKVFullDecoder, upload_workload
+    from sparse_long_context_08_b300.workloads import CONFIGS, make_workload
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    E.lib()
+    w = make_workload(args.workload, seed=CONFIGS[args.workload]["seed"] + 1000 * rank,
+                      **overrides(args))
+    kv, q = upload_workload(w)
+    dec = EntmaxKVFullDecoder(kv, w.num_q_heads, float(w.scale), w.alpha)
+    torch.cuda.synchronize()
+    flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device="cuda")
+    flush_read = torch.ones(max(1, args.flush_mb // 2) << 20, dtype=torch.uint8, device="cuda")
+
+    def flush_l2(i):
+        flush.fill_(i & 255)
+        flush_read.sum(dtype=torch.int32)
+
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    for x in evs:
+        x.record()
+    torch.cuda.synchronize()
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap_stream):
+        for _ in range(2):
+            dec.decode(q)
+    torch.cuda.current_stream().wait_stream(cap_stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap_stream):
+        dec.decode(q)
+    staged = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(staged, stream=cap_stream):
+        E.entmaxkv_set_stage_events(evs)
+        dec.decode(q)
+        E.entmaxkv_set_stage_events(None)
+    torch.cuda.synchronize()
+    for i in range(max(3, args.warmup)):
+        graph.replay()
+        staged.replay()
+        flush_l2(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    K = args.steps
+    names = ["plan", "qk", "tpv"]
+    stage = {n: [] for n in names}
+    total = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(bus_id_of(local_rank)) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    torch.cuda.synchronize()
+    for i in range(K):
+        t_start.record()
+        graph.replay()
+        t_end.record()
+        torch.cuda.synchronize()
+        total.append(t_start.elapsed_time(t_end))
+        flush_l2(i + 7)
+    for i in range(min(K, 50)):
+        staged.replay()
+        torch.cuda.synchronize()
+        for j, n_ in enumerate(names):
+            stage[n_].append(evs[j].elapsed_time(evs[j + 1]))
+        flush_l2(i + 3)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    t_sum = torch.tensor([sum(total)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t_sum, op=dist.ReduceOp.MAX)
+    ms_per_step = float(t_sum.item()) / K
+
+    up, vr = E.entmaxkv_decode_counts(dec.workspace, w.batch, w.num_q_heads, w.num_kv_heads,
+                                      w.head_dim, w.page_size, w.max_pages, w.max_pages)
+    esz = 2 if w.dtype == "bf16" else 4
+    page_bytes = w.page_size * w.head_dim * esz
+    bytes_k = int(up.sum()) * page_bytes
+    bytes_v = int(vr.sum()) * w.head_dim * esz
+    small = 2 * w.batch * w.num_q_heads * w.head_dim * 4 + w.batch * w.max_pages * 4
+    bytes_step = bytes_k + bytes_v + small
+    mean = {n: statistics.mean(v) for n, v in stage.items()}
+    dom = max(mean, key=mean.get)
+    peak, peak_kind = measured_peak()
+    dom_bytes = {"qk": bytes_k, "tpv": bytes_v}.get(dom)
+    achieved = dom_bytes / (mean[dom] * 1e-3) / 1e9 if dom_bytes else None
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+                "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                "algorithmic_bytes": dom_bytes}
+
+    e2e = None
+    if not args.no_e2e:
+        q_host = q.cpu().pin_memory()
+        out_host = torch.empty(dec.out.shape, dtype=torch.float32).pin_memory()
+        q_dev = torch.empty_like(q)
+        for _ in range(3):
+            dec.step_host(q_host, out_host, q_dev)
+            stream.synchronize()
+        times = []
+        for i in range(min(K, 100)):
+            flush_l2(i)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            dec.step_host(q_host, out_host, q_dev)
+            stream.synchronize()
+            times.append(time.perf_counter() - t0)
+        t_e2e = torch.tensor([sum(times) / len(times)], dtype=torch.float64, device="cuda")
+        if world > 1:
+            dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
+        e2e = {"value": float(t_e2e.item()) / world * 1e6, "unit": "us/step",
+               "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4,
+               "timing": "host wall clock per step incl. H2D, the call, D2H and sync"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us, desc, cores = oracle_full_time_per_step(w, args.cpu_seconds)
+        cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": FULL_METRIC, "value": ms_per_step * 1e3 / world, "unit": "us/step",
+        "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": dict(workload_config(w), mode="full-cache"),
+        "hbm_gbs": bytes_step / (ms_per_step * 1e-3) / 1e9,
+        "hbm_frac_of_measured": bytes_step / (ms_per_step * 1e-3) / 1e9 / peak,
+        "bytes_per_step": bytes_step,
+        "bytes_breakdown": {"k_all_pages": bytes_k, "v_support_rows": bytes_v,
+                            "q_out_page_table": small, "pages": int(up.sum()),
+                            "v_rows": int(vr.sum())},
+        "stage_us": {n: v * 1e3 for n, v in mean.items()},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 3 * K, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.mode == "full":
+        run_full(args)
     else:
         run_ours(args)
 

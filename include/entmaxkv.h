@@ -154,6 +154,27 @@ int entmaxkv_decode(const float* q, int32_t num_q_heads, float scale,
                     float* out, float* tau_out, int32_t* support_out,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* Full-cache alpha-entmax decode, the exact attention the sparse decode
+ * approximates ([EntmaxKV] §1 and §3: sparse output equals it whenever the
+ * kept pages hold its support).  For each (b, h): every valid token of
+ * sequence b is scored z = scale q.k, tau is the exact alpha-entmax threshold of
+ * (alpha-1) z over all of them (same solver as entmaxkv_decode) and out =
+ * sum_i p_i v_i / sum_i p_i.  Each kv head's whole cache is read once for its
+ * query group; only the V rows of tokens with p_i > 0 are read.
+ * Arguments, outputs and errors as entmaxkv_decode without the selection;
+ * workspace: at least entmaxkv_full_workspace_size(...) bytes, 256-byte
+ * aligned, not shared with a concurrent call. */
+int entmaxkv_decode_full(const float* q, int32_t num_q_heads, float scale,
+                         const ekv_paged_kv* kv, float alpha, float* out,
+                         float* tau_out, int32_t* support_out, void* workspace,
+                         size_t ws_bytes, void* stream);
+
+/* Host-only: bytes of workspace entmaxkv_decode_full needs for these sizes
+ * (0 if the sizes are invalid). */
+size_t entmaxkv_full_workspace_size(int32_t batch, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t page_size, int32_t max_pages);
+
 /* Bytes of the scratch array built into the library for
  * entmaxkv_decode_noalloc. */
 #define ENTMAXKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)

@@ -90,3 +90,39 @@ class EntmaxKVDecoder:
             q_dev.copy_(q_host, non_blocking=True)
             self.step(q_dev, s)
             out_host.copy_(self.out, non_blocking=True)
+
+
+class EntmaxKVFullDecoder:
+    """Full-cache alpha-entmax decode: attention over every valid token, the
+    exact result the sparse pipeline approximates."""
+
+    def __init__(self, kv: E.PagedKV, num_q_heads: int, scale: float, alpha: float):
+        self.kv = kv
+        self.Hq = int(num_q_heads)
+        self.scale = float(scale)
+        self.alpha = float(alpha)
+        dev = kv.k_pool.device
+        B, Hq = kv.batch, self.Hq
+        self.out = torch.empty((B, Hq, kv.head_dim), dtype=torch.float32, device=dev)
+        self.tau = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        self.support = torch.empty((B, Hq), dtype=torch.int32, device=dev)
+        ws = E.entmaxkv_full_workspace_size(B, Hq, kv.num_kv_heads, kv.head_dim, kv.page_size,
+                                            kv.max_pages)
+        if ws == 0:
+            raise ValueError("invalid sizes for the full-cache workspace")
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def decode(self, q: torch.Tensor, stream=None) -> torch.Tensor:
+        E.entmaxkv_decode_full(q, self.Hq, self.scale, self.kv, self.alpha, self.out, self.tau,
+                               self.support, self.workspace, stream)
+        return self.out
+
+    def step_host(self, q_host: torch.Tensor, out_host: torch.Tensor, q_dev: torch.Tensor,
+                  stream=None) -> None:
+        """q_host (pinned) -> device, the full-cache decode, out -> out_host
+        (pinned).  Asynchronous on `stream`."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            q_dev.copy_(q_host, non_blocking=True)
+            self.decode(q_dev, s)
+            out_host.copy_(self.out, non_blocking=True)

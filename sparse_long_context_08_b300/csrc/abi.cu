@@ -155,7 +155,6 @@ static int decode_impl(const float* q, int32_t num_q_heads, float scale, const e
     if (!std::isfinite(scale) || !(scale > 0.f) || !is_alpha(alpha)) return EKV_INVALID_ARG;
     if (cap_pages < 1) return EKV_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EKV_INVALID_ARG;
-    if ((int64_t)cap_pages * kv->page_size > 16384) return EKV_UNSUPPORTED;
     if ((int64_t)kv->max_pages > ekv::kMaxPagesTopk) return EKV_UNSUPPORTED;
     if ((int64_t)kv->num_blocks * kv->num_kv_heads * kv->page_size > INT32_MAX) return EKV_UNSUPPORTED;
     const ekv::DecodeLayout L = ekv::decode_layout(kv->batch, num_q_heads, kv->num_kv_heads,
@@ -173,6 +172,32 @@ int entmaxkv_decode(const float* q, int32_t num_q_heads, float scale, const ekv_
                     size_t ws_bytes, void* stream) {
     return decode_impl(q, num_q_heads, scale, kv, sel, n_sel, cap_pages, alpha, out, tau_out,
                        support_out, workspace, ws_bytes, stream);
+}
+
+size_t entmaxkv_full_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t page_size, int32_t max_pages) {
+    return entmaxkv_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                                   max_pages, max_pages);
+}
+
+int entmaxkv_decode_full(const float* q, int32_t num_q_heads, float scale, const ekv_paged_kv* kv,
+                         float alpha, float* out, float* tau_out, int32_t* support_out,
+                         void* workspace, size_t ws_bytes, void* stream) {
+    int st = check_kv(kv, true, true);
+    if (st) return st;
+    if ((st = check_heads(kv, num_q_heads))) return st;
+    if (!q || !out || !workspace) return EKV_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f) || !is_alpha(alpha)) return EKV_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EKV_INVALID_ARG;
+    if ((int64_t)kv->max_pages > ekv::kMaxPagesTopk) return EKV_UNSUPPORTED;
+    if ((int64_t)kv->num_blocks * kv->num_kv_heads * kv->page_size > INT32_MAX) return EKV_UNSUPPORTED;
+    const ekv::DecodeLayout L = ekv::decode_layout(kv->batch, num_q_heads, kv->num_kv_heads,
+                                                   kv->head_dim, kv->page_size, kv->max_pages,
+                                                   kv->max_pages);
+    if (ws_bytes < L.total) return EKV_WORKSPACE_TOO_SMALL;
+    return from_cuda(ekv::launch_decode_full(q, num_q_heads, scale, to_kv(kv), alpha, out, tau_out,
+                                             support_out, workspace, L,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 int entmaxkv_set_stage_events(void* const* events, int32_t n_events) {

@@ -64,6 +64,12 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, 
     L.vrows = take(sizeof(int) * L.U);
     L.z = take(sizeof(float) * (size_t)L.U * L.G * L.Umax * P);
     L.tau = take(sizeof(float) * (size_t)B * Hq);
+    L.ccap = cap * P;
+    L.cand_x = L.cand_pos = 0;
+    if (L.ccap > kTpvSmemCand) {
+        L.cand_x = take(sizeof(float) * (size_t)B * Hq * L.ccap);
+        L.cand_pos = take(sizeof(int) * (size_t)B * Hq * L.ccap);
+    }
     L.total = o;
     return L;
 }
@@ -82,6 +88,40 @@ plan_kernel(KV kv, int Hq, const int32_t* __restrict__ sel, const int32_t* __res
     const int nwm = (kv.maxp + 31) / 32;
     build_plan<G>(kv, Hq, sel, n_sel, cap, ws, L, blockIdx.x, s_plan,
                   reinterpret_cast<int*>(s_plan + (size_t)G * nwm), red, s_ns);
+}
+
+// Plan of the full-cache decode: the union of unit u is every valid page of
+// its sequence, selected by all G heads.  Grid (U, chunks): chunk c writes
+// pages [c kPlanAllChunk, +kPlanAllChunk) and resets its share of the unit's
+// per-call state (as build_plan does).
+constexpr int kPlanAllChunk = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_all_kernel(KV kv, int Hq, WS ws, DecodeLayout L) {
+    pdl_enter();
+    const int u = blockIdx.x, c = blockIdx.y, nc = gridDim.y;
+    const int b = u / kv.hkv, kvh = u - b * kv.hkv;
+    const int G = L.G;
+    const int np = pages_of(kv, b);
+    if (c == 0 && threadIdx.x < G) ws.head_max[b * Hq + kvh * G + threadIdx.x] = 0u;
+    const int wpc = (L.nvw + nc - 1) / nc;
+    for (int i = c * wpc + threadIdx.x; i < min(L.nvw, (c + 1) * wpc); i += blockDim.x)
+        ws.vtok[(int64_t)u * L.nvw + i] = 0u;
+    int* upage = ws.union_page + (int64_t)u * L.Umax;
+    int* umask = ws.union_mask + (int64_t)u * L.Umax;
+    int* ublk = ws.union_blk + (int64_t)u * L.Umax;
+    const int i1 = min(np, (c + 1) * kPlanAllChunk);
+    for (int i = c * kPlanAllChunk + threadIdx.x; i < i1; i += blockDim.x) {
+        int blk = kv.pt[(int64_t)b * kv.maxp + i];
+        if (blk < 0 || blk >= kv.nb) {
+            flag_bad_data();
+            blk = -1;
+        }
+        upage[i] = i;
+        umask[i] = (1 << G) - 1;
+        ublk[i] = blk;
+    }
+    if (c == 0 && threadIdx.x == 0) ws.union_count[u] = np;
 }
 
 // ---------------------------------------------------------------------------
@@ -788,6 +828,195 @@ __global__ void count_rows_kernel(WS ws, DecodeLayout L) {
 }
 
 // ---------------------------------------------------------------------------
+// tpv over global candidate buffers: the same steps as tpv_kernel for heads
+// whose selection (or the whole cache) holds more candidates than shared
+// memory does.  Candidates, then weights, live in the head's ccap-entry slice
+// of cand_x / cand_pos; every threshold iteration re-reads them (L2).
+// ---------------------------------------------------------------------------
+constexpr int kTpvgRows = 4;          // V rows in flight per row group
+
+template <typename T, int D, int E>
+__global__ void __launch_bounds__(kTpvThreads)
+tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __restrict__ out,
+                  float* __restrict__ tau_out, int32_t* __restrict__ support_out) {
+    pdl_enter();
+    constexpr int EPC = Elem<T>::kPer16;
+    constexpr int LPR = D / EPC;              // lanes per V row
+    constexpr int RG = kTpvThreads / LPR;     // row groups
+    __shared__ float s_red[RG * D];
+    __shared__ float fred[40];
+    __shared__ float2 f2red[32];
+    __shared__ int ired[40];
+
+    const int G = L.G;
+    const int Hkv = Hq / G;
+    const int bh = blockIdx.x;
+    const int b = bh / Hq;
+    const int h = bh - b * Hq;
+    const int kvh = h / G;
+    const int hg = h - kvh * G;
+    const int u = b * Hkv + kvh;
+    const int tid = threadIdx.x;
+    const int P = kv.P;
+    const float* z = ws.z + ((int64_t)u * G + hg) * L.Umax * P;
+    float* cx = ws.cand_x + (int64_t)bh * L.ccap;
+    int* cp = ws.cand_pos + (int64_t)bh * L.ccap;
+    float* outb = out + (int64_t)bh * D;
+
+    const uint32_t key = __ldcg(ws.head_max + bh);
+    const int ucnt = __ldcg(ws.union_count + u);
+    const int n = ucnt * P;
+    if (key == 0u || n == 0) {
+        for (int i = tid; i < D; i += blockDim.x) outb[i] = 0.f;
+        if (tid == 0) {
+            ws.tau[bh] = INFINITY;
+            if (tau_out) tau_out[bh] = INFINITY;
+            if (support_out) support_out[bh] = 0;
+        }
+        return;
+    }
+    const float mx = key_float(key);
+
+    // candidates x = z' - max > -1, compacted in a fixed thread order
+    int m = 0;
+    for (int t0 = 0; t0 < n; t0 += kTpvTile) {
+        float v[kTpvVec * 4];
+#pragma unroll
+        for (int j = 0; j < kTpvVec; ++j) {
+            const int i = t0 + (j * kTpvThreads + tid) * 4;
+            const float4 f = i < n ? __ldcg(reinterpret_cast<const float4*>(z + i))
+                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+        }
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < kTpvVec * 4; ++j) {
+            const int i = t0 + ((j >> 2) * kTpvThreads + tid) * 4 + (j & 3);
+            v[j] = i < n ? v[j] - mx : -INFINITY;
+            c += v[j] > -1.f;
+        }
+        int tot;
+        int pos = m + block_exclusive_scan(c, ired, &tot);
+#pragma unroll
+        for (int j = 0; j < kTpvVec * 4; ++j) {
+            if (v[j] > -1.f) {
+                if (pos < L.ccap) {
+                    cx[pos] = v[j];
+                    cp[pos] = t0 + ((j >> 2) * kTpvThreads + tid) * 4 + (j & 3);
+                }
+                ++pos;
+            }
+        }
+        m += tot;
+    }
+    if (m > L.ccap) {                  // cannot happen: candidates are selected tokens
+        if (tid == 0) flag_bad_data();
+        m = L.ccap;
+    }
+    __syncthreads();                   // the block's candidate writes are visible
+
+    // threshold t (relative to the max): f(t) = sum (x - t)_+^e - 1 = 0
+    float t;
+    if (E != 0) {
+        t = -1.f;
+        for (int it = 0; it < 64; ++it) {
+            float2 acc = make_float2(0.f, 0.f);
+            for (int i = tid; i < m; i += blockDim.x) {
+                const float a = __ldcg(cx + i) - t;
+                if (a > 0.f) {
+                    if (E == 2) { acc.x = fmaf(a, a, acc.x); acc.y += a; }
+                    else { acc.x += a; acc.y += 1.f; }
+                }
+            }
+            acc = block_sum2(acc, f2red);
+            const float dv = E == 2 ? 2.f * acc.y : acc.y;
+            if (!(dv > 0.f)) break;
+            const float step = (acc.x - 1.f) / dv;
+            t += step;
+            if (!(step > 1e-7f)) break;
+        }
+    } else {
+        const float ex = 1.f / (alpha - 1.f);
+        float lo = -1.f, hi = -powf(static_cast<float>(m), 1.f - alpha);
+        for (int it = 0; it < 48; ++it) {
+            const float mid = 0.5f * (lo + hi);
+            float f = 0.f;
+            for (int i = tid; i < m; i += blockDim.x) {
+                const float a = __ldcg(cx + i) - mid;
+                if (a > 0.f) f += powf(a, ex);
+            }
+            f = block_sum(f, fred) - 1.f;
+            if (f >= 0.f) lo = mid; else hi = mid;
+        }
+        t = 0.5f * (lo + hi);
+    }
+
+    // weights in place; V row of each support token
+    const float ex = 1.f / (alpha - 1.f);
+    const T* vbase = static_cast<const T*>(kv.v);
+    int sup = 0;
+    float wsum = 0.f;
+    for (int i = tid; i < m; i += blockDim.x) {
+        const float a = cx[i] - t;
+        const float w = a > 0.f ? pow_e(a, E, ex) : 0.f;
+        cx[i] = w;
+        if (w > 0.f) {
+            ++sup;
+            wsum += w;
+            const int pos = cp[i];
+            const int ui = pos / P;
+            const int blk = __ldcg(ws.union_blk + (int64_t)u * L.Umax + ui);
+            cp[i] = blk >= 0 ? ((blk * Hkv + kvh) * P + (pos - ui * P)) : -1;
+            atomicOr(&ws.vtok[(int64_t)u * L.nvw + (pos >> 5)], 1u << (pos & 31));
+        }
+    }
+    sup = block_sum_i(sup, ired);
+    wsum = block_sum(wsum, fred);      // includes a barrier: weights and rows are visible
+
+    const int lr = tid % LPR;
+    const int rg = tid / LPR;
+    float acc[EPC];
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
+    for (int i0 = rg; i0 < m; i0 += RG * kTpvgRows) {
+        float w[kTpvgRows];
+        int row[kTpvgRows];
+#pragma unroll
+        for (int k = 0; k < kTpvgRows; ++k) {
+            const int i = i0 + k * RG;
+            w[k] = i < m ? __ldcg(cx + i) : 0.f;
+            row[k] = i < m ? __ldcg(cp + i) : -1;
+        }
+        uint4 r[kTpvgRows];
+#pragma unroll
+        for (int k = 0; k < kTpvgRows; ++k)
+            if (w[k] > 0.f && row[k] >= 0) r[k] = ld_nc_v4(vbase + (int64_t)row[k] * D + lr * EPC);
+#pragma unroll
+        for (int k = 0; k < kTpvgRows; ++k)
+            if (w[k] > 0.f && row[k] >= 0) {
+                float x[EPC];
+                Elem<T>::widen(r[k], x);
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc[e] = fmaf(w[k], x[e], acc[e]);
+            }
+    }
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) s_red[rg * D + lr * EPC + e] = acc[e];
+    __syncthreads();
+    for (int d = tid; d < D; d += blockDim.x) {
+        float o = 0.f;
+        for (int r = 0; r < RG; ++r) o += s_red[r * D + d];
+        outb[d] = wsum > 0.f ? o / wsum : 0.f;
+    }
+    if (tid == 0) {
+        const float tau = t + mx;
+        ws.tau[bh] = tau;
+        if (tau_out) tau_out[bh] = tau;
+        if (support_out) support_out[bh] = sup;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
 static cudaEvent_t g_stage_events[4];
@@ -843,8 +1072,18 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
                               int32_t* support_out, cudaStream_t s) {
     constexpr int RG = kTpvThreads / (D / Elem<T>::kPer16);
     const int cand_cap = cap * kv.P;
+    cudaError_t e;
+    if (cand_cap > kTpvSmemCand) {
+        if (!ws.cand_x || L.ccap < cand_cap) return cudaErrorInvalidValue;
+        stage_mark(2, s);
+        e = launch_pdl(tpv_global_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvThreads), 0, s, Hq,
+                       alpha, kv, ws, L, out, tau_out, support_out);
+        if (e != cudaSuccess) return e;
+        stage_mark(3, s);
+        return cudaSuccess;
+    }
     const size_t smem = (size_t)cand_cap * 8 + (size_t)RG * D * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(tpv_kernel<T, D, E>,
+    e = cudaFuncSetAttribute(tpv_kernel<T, D, E>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     stage_mark(2, s);
@@ -855,22 +1094,12 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
     return cudaSuccess;
 }
 
+// qk and tpv after a plan: scores of the union pages, then threshold and values.
 template <typename T, int D, int G>
-static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV& kv,
-                                   const int32_t* sel, const int32_t* n_sel, int cap, float alpha,
-                                   float* out, float* tau_out, int32_t* support_out, const WS& ws,
-                                   const DecodeLayout& L, cudaStream_t s) {
+static cudaError_t launch_qk_tpv(const float* q, int Hq, float scale, const KV& kv, int cap,
+                                 float alpha, float* out, float* tau_out, int32_t* support_out,
+                                 const WS& ws, const DecodeLayout& L, cudaStream_t s) {
     cudaError_t e;
-    if (L.U > kMaxUnits || cap > kPlanSelRegs * kPlanThreads / G) return cudaErrorInvalidValue;
-    stage_mark(0, s);
-    {
-        const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax);
-        e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel,
-                       cap, ws, L);
-        if (e != cudaSuccess) return e;
-    }
     if constexpr (sizeof(T) == 2) {
         const int page_bytes = kv.P * D * 2;
         const int ns = std::min(8, kQmStageBytes / page_bytes);
@@ -903,6 +1132,38 @@ static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV
     return launch_tpv<0, T, D>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
 }
 
+template <typename T, int D, int G>
+static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV& kv,
+                                   const int32_t* sel, const int32_t* n_sel, int cap, float alpha,
+                                   float* out, float* tau_out, int32_t* support_out, const WS& ws,
+                                   const DecodeLayout& L, cudaStream_t s) {
+    cudaError_t e;
+    if (L.U > kMaxUnits || cap > kPlanSelRegs * kPlanThreads / G) return cudaErrorInvalidValue;
+    stage_mark(0, s);
+    const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax);
+    e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel, cap,
+                   ws, L);
+    if (e != cudaSuccess) return e;
+    return launch_qk_tpv<T, D, G>(q, Hq, scale, kv, cap, alpha, out, tau_out, support_out, ws, L, s);
+}
+
+template <typename T, int D, int G>
+static cudaError_t launch_decode_full_t(const float* q, int Hq, float scale, const KV& kv,
+                                        float alpha, float* out, float* tau_out,
+                                        int32_t* support_out, const WS& ws, const DecodeLayout& L,
+                                        cudaStream_t s) {
+    if (L.U > kMaxUnits || L.Umax != kv.maxp) return cudaErrorInvalidValue;
+    stage_mark(0, s);
+    const int chunks = (kv.maxp + kPlanAllChunk - 1) / kPlanAllChunk;
+    cudaError_t e = launch_pdl(plan_all_kernel, dim3(L.U, chunks), dim3(kPlanThreads), 0, s, kv, Hq,
+                               ws, L);
+    if (e != cudaSuccess) return e;
+    return launch_qk_tpv<T, D, G>(q, Hq, scale, kv, kv.maxp, alpha, out, tau_out, support_out, ws,
+                                  L, s);
+}
+
 cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, const int32_t* sel,
                           const int32_t* n_sel, int cap, float alpha, float* out, float* tau_out,
                           int32_t* support_out, void* ws_base, const DecodeLayout& L,
@@ -912,6 +1173,18 @@ cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, con
     EKV_DISPATCH_T(kv.dtype, EKV_DISPATCH_D(kv.D, EKV_DISPATCH_G(G, {
         return launch_decode_t<T, kD, kG>(q, Hq, scale, kv, sel, n_sel, cap, alpha, out, tau_out,
                                            support_out, ws, L, s);
+    })))
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_full(const float* q, int Hq, float scale, const KV& kv, float alpha,
+                               float* out, float* tau_out, int32_t* support_out, void* ws_base,
+                               const DecodeLayout& L, cudaStream_t s) {
+    const WS ws = ws_views(ws_base, L);
+    const int G = L.G;
+    EKV_DISPATCH_T(kv.dtype, EKV_DISPATCH_D(kv.D, EKV_DISPATCH_G(G, {
+        return launch_decode_full_t<T, kD, kG>(q, Hq, scale, kv, alpha, out, tau_out, support_out,
+                                                ws, L, s);
     })))
     return cudaErrorInvalidValue;
 }

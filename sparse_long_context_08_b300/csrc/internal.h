@@ -28,12 +28,16 @@ struct KV {
 // pages (at most Umax of them) once.  Scores are kept per unit in union order,
 // [U][G][Umax * P], with -inf where a head did not select the page; the
 // physical block of every union page is kept for the value stage.  vtok marks,
-// per unit, the tokens whose V row was read (nvw words per unit).
+// per unit, the tokens whose V row was read (nvw words per unit).  When a
+// head's selection (cap * P tokens) is larger than the threshold kernel keeps
+// in shared memory, the candidates go to per-head global buffers of ccap =
+// cap * P entries (cand_x, cand_pos; absent otherwise).
 struct DecodeLayout {
-    int    U, G, Umax, nvw;
+    int    U, G, Umax, nvw, ccap;
     size_t union_count, head_max, union_page, union_mask, union_blk, vtok, vrows;
-    size_t z, tau, total;
+    size_t z, tau, cand_x, cand_pos, total;
 };
+constexpr int kTpvSmemCand = 16384;      // candidates per head the shared-memory threshold kernel holds
 DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap);
 
 cudaError_t launch_build_meta(const KV& kv, int first_page, int num_pages, void* kmin,
@@ -50,6 +54,11 @@ cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, 
 cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, const int32_t* sel,
                           const int32_t* n_sel, int cap, float alpha, float* out, float* tau_out,
                           int32_t* support_out, void* ws, const DecodeLayout& L, cudaStream_t s);
+// Full-cache decode: every valid token of every sequence, for all heads
+// (workspace laid out by decode_layout(..., cap = max_pages)).
+cudaError_t launch_decode_full(const float* q, int Hq, float scale, const KV& kv, float alpha,
+                               float* out, float* tau_out, int32_t* support_out, void* ws,
+                               const DecodeLayout& L, cudaStream_t s);
 
 // Optional events recorded between the decode kernels (plan | qk | tpv):
 // events[0] before plan, [1] before qk, [2] before tpv, [3] after tpv.

@@ -21,6 +21,8 @@ struct WS {
     int* vrows;           // per-unit popcount of vtok (measurement)
     float* z;             // [U][G][Umax * P]
     float* tau;
+    float* cand_x;        // [B * Hq][ccap] candidates, then weights (large selections only)
+    int* cand_pos;        // [B * Hq][ccap] their score index, then V row
 };
 inline WS ws_views(void* base, const DecodeLayout& L) {
     char* c = static_cast<char*>(base);
@@ -28,7 +30,9 @@ inline WS ws_views(void* base, const DecodeLayout& L) {
               reinterpret_cast<int*>(c + L.union_page), reinterpret_cast<int*>(c + L.union_mask),
               reinterpret_cast<int*>(c + L.union_blk), reinterpret_cast<uint32_t*>(c + L.vtok),
               reinterpret_cast<int*>(c + L.vrows), reinterpret_cast<float*>(c + L.z),
-              reinterpret_cast<float*>(c + L.tau)};
+              reinterpret_cast<float*>(c + L.tau),
+              L.cand_x ? reinterpret_cast<float*>(c + L.cand_x) : nullptr,
+              L.cand_pos ? reinterpret_cast<int*>(c + L.cand_pos) : nullptr};
 }
 
 __device__ __forceinline__ int pages_of(const KV& kv, int b) {

@@ -30,7 +30,8 @@ EKV_SELECT_GAUSS = 1
 SYMBOLS = ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select",
            "entmaxkv_decode", "entmaxkv_workspace_size", "entmaxkv_status_string",
            "entmaxkv_read_device_status", "entmaxkv_version", "entmaxkv_set_stage_events",
-           "entmaxkv_decode_counts", "entmaxkv_decode_noalloc")
+           "entmaxkv_decode_counts", "entmaxkv_decode_noalloc", "entmaxkv_decode_full",
+           "entmaxkv_full_workspace_size")
 
 
 class EntmaxKVError(RuntimeError):
@@ -76,9 +77,13 @@ def lib() -> C.CDLL:
         L.entmaxkv_version.restype = i32
         L.entmaxkv_set_stage_events.argtypes = [vp, i32]
         L.entmaxkv_decode_counts.argtypes = [vp] + [i32] * 7 + [vp, vp, vp]
+        L.entmaxkv_decode_full.argtypes = [vp, i32, f32, vp, f32, vp, vp, vp, vp, sz, vp]
+        L.entmaxkv_full_workspace_size.argtypes = [i32] * 6
+        L.entmaxkv_full_workspace_size.restype = sz
         for name in ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select",
                      "entmaxkv_decode", "entmaxkv_read_device_status",
-                     "entmaxkv_set_stage_events", "entmaxkv_decode_counts", "entmaxkv_decode_noalloc"):
+                     "entmaxkv_set_stage_events", "entmaxkv_decode_counts", "entmaxkv_decode_noalloc",
+                     "entmaxkv_decode_full"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -278,6 +283,30 @@ def entmaxkv_decode(q: torch.Tensor, num_q_heads: int, scale: float, kv: PagedKV
                                  _ptr(n_sel), cap_pages, float(alpha), _ptr(out), _ptr(tau_out),
                                  _ptr(support_out), _ptr(workspace), workspace.numel(),
                                  _stream(stream)))
+
+
+def entmaxkv_full_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                                 max_pages) -> int:
+    return int(lib().entmaxkv_full_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                  page_size, max_pages))
+
+
+def entmaxkv_decode_full(q: torch.Tensor, num_q_heads: int, scale: float, kv: PagedKV,
+                         alpha: float, out: torch.Tensor, tau_out: torch.Tensor | None,
+                         support_out: torch.Tensor | None, workspace: torch.Tensor,
+                         stream=None) -> None:
+    """Full-cache alpha-entmax decode: every valid token of every sequence."""
+    _need(q, "q", torch.float32, (kv.batch, num_q_heads, kv.head_dim))
+    _need(out, "out", torch.float32, (kv.batch, num_q_heads, kv.head_dim))
+    if tau_out is not None:
+        _need(tau_out, "tau_out", torch.float32, (kv.batch, num_q_heads))
+    if support_out is not None:
+        _need(support_out, "support_out", torch.int32, (kv.batch, num_q_heads))
+    _need(workspace, "workspace", torch.uint8)
+    _check("entmaxkv_decode_full",
+           lib().entmaxkv_decode_full(_ptr(q), num_q_heads, float(scale), kv.ref, float(alpha),
+                                      _ptr(out), _ptr(tau_out), _ptr(support_out),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def entmaxkv_read_device_status(stream=None) -> int:

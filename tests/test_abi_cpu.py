@@ -54,6 +54,18 @@ def test_workspace_size_is_host_only_and_monotone(L):
     assert L.entmaxkv_workspace_size(0, 32, 8, 128, 32, 4096, 128) == 0
 
 
+def test_full_workspace_size_matches_a_whole_cache_selection(L):
+    # the full-cache decode selects every page: its workspace is the decode
+    # workspace at cap = max_pages, with per-head candidate buffers once the
+    # cache holds more tokens than the shared-memory threshold kernel keeps
+    f = L.entmaxkv_full_workspace_size(8, 32, 8, 128, 32, 4096)
+    assert f == L.entmaxkv_workspace_size(8, 32, 8, 128, 32, 4096, 4096)
+    assert f >= 8 * 32 * 4096 * 32 * 8          # candidates + positions, 8 B per token
+    assert L.entmaxkv_full_workspace_size(8, 30, 8, 128, 32, 4096) == 0
+    small = L.entmaxkv_workspace_size(1, 8, 8, 64, 16, 64, 64)      # 1024 tokens: no buffers
+    assert small < 8 * 64 * 16 * 8 + L.entmaxkv_workspace_size(1, 8, 8, 64, 16, 64, 63)
+
+
 def _kv(**over):
     from sparse_long_context_08_b300.entmaxkv import _PagedKV
     f = dict(k_pool=16, v_pool=16, dtype=1, num_blocks=4, num_kv_heads=1, page_size=16,
@@ -109,6 +121,17 @@ def test_invalid_arguments_are_rejected_before_any_launch(L):
     assert lib.entmaxkv_build_page_meta(ref, 0, 4, C.byref(empty), 0, 0,
                                         None) == L.EKV_INVALID_ARG
     assert lib.entmaxkv_read_device_status(None, None) == L.EKV_INVALID_ARG
+    # full-cache decode: same checks as decode, no selection
+    assert lib.entmaxkv_decode_full(nz, 1, 1.0, None, 1.5, nz, None, None, C.c_void_p(256),
+                                    1 << 30, None) == L.EKV_INVALID_ARG
+    assert lib.entmaxkv_decode_full(nz, 1, 1.0, ref, 1.0, nz, None, None, C.c_void_p(256),
+                                    1 << 30, None) == L.EKV_INVALID_ARG
+    assert lib.entmaxkv_decode_full(nz, 1, 1.0, ref, 1.5, nz, None, None, C.c_void_p(272),
+                                    1 << 30, None) == L.EKV_INVALID_ARG
+    assert lib.entmaxkv_decode_full(nz, 1, 1.0, ref, 1.5, nz, None, None, C.c_void_p(256),
+                                    16, None) == L.EKV_WORKSPACE_TOO_SMALL
+    assert lib.entmaxkv_decode_full(nz, 3, 1.0, ref, 1.5, nz, None, None, C.c_void_p(256),
+                                    1 << 30, None) == L.EKV_UNSUPPORTED      # group of 3
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):

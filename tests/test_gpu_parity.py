@@ -133,6 +133,58 @@ def test_full_size_sampled_heads(name, alpha):
 
 
 # ---------------------------------------------------------------------------
+# full-cache decode (every valid token) against the oracle's full attention
+# ---------------------------------------------------------------------------
+
+def full_cache_parity(w, heads=None):
+    from sparse_long_context_08_b300.api import EntmaxKVFullDecoder, upload_workload
+    kv_d, q = upload_workload(w)
+    dec = EntmaxKVFullDecoder(kv_d, w.num_q_heads, float(w.scale), w.alpha)
+    dec.decode(q)
+    torch.cuda.synchronize()
+    BH = w.batch * w.num_q_heads
+    out = dec.out.cpu().numpy().astype(np.float64).reshape(BH, -1)
+    tau = dec.tau.cpu().numpy().astype(np.float64).reshape(BH)
+    sup = dec.support.cpu().numpy().reshape(BH)
+    hs = list(range(BH)) if heads is None else list(heads)
+    kv = oracle.KV(w)
+    f = oracle.decode_full(kv, float(w.scale), w.alpha, heads=hs)
+    compare_decode(out, tau, f.out, f.tau, hs, sup, f.support)
+    assert E.entmaxkv_read_device_status() == E.EKV_OK
+    return sup[hs]
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", {}),
+    ("tiny", {"seq_lens": [4096 - 7], "context": 4089}),
+    ("gqa32k", {"batch": 2, "seq_lens": [8192, 5000]}),
+    ("long128k", {"batch": 2, "seq_lens": [16384, 12345]}),
+    ("long128k", {"batch": 2, "seq_lens": [16384, 12345], "alpha": 2.0}),
+    ("long128k", {"batch": 1, "context": 8192, "alpha": 1.3, "seed": 7}),
+    ("gauss64k", {"batch": 2, "seq_lens": [16384, 9999]}),
+])
+def test_full_cache_reduced(name, over):
+    full_cache_parity(make_workload(name, **over))
+
+
+@pytest.mark.parametrize("name", ["gqa32k", "long128k", "ctx1m"])
+def test_full_cache_full_size_sampled_heads(name):
+    w = make_workload(name)
+    full_cache_parity(w, heads=sampled_heads(w, 48))
+    torch.cuda.empty_cache()
+
+
+def test_large_selection_uses_global_candidates():
+    """A budget larger than the shared-memory candidate buffer (cap * P >
+    16384 tokens) goes through the global-buffer threshold kernel: same
+    parity with the oracle on the same selection."""
+    w = make_workload("long128k", batch=2, seq_lens=[32768 * 2, 40000], budget_tokens=32768,
+                      planted_pages=4)
+    assert w.cap_pages * w.page_size > 16384
+    full_parity(w)
+
+
+# ---------------------------------------------------------------------------
 # shapes: head_dim, dtype, group size, page size, general alpha
 # ---------------------------------------------------------------------------
 

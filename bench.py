@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="long128k")
     ap.add_argument("--alpha", type=float, default=None)
+    ap.add_argument("--policy", choices=["topk", "gauss", "topk_shared"], default=None,
+                    help="override the workload's selection policy")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
     ap.add_argument("--context", type=int, default=None, help="override the context length")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -59,6 +61,8 @@ def overrides(args) -> dict:
     kw = {}
     if args.alpha is not None:
         kw["alpha"] = args.alpha
+    if args.policy is not None:
+        kw["policy"] = args.policy
     if args.batch is not None:
         kw["batch"] = args.batch
     if args.context is not None:
@@ -383,7 +387,7 @@ def run_ours(args):
     esz = 2 if w.dtype == "bf16" else 4
     pages = sum(w.pages_of(b) for b in range(w.batch))
     page_bytes = w.page_size * w.head_dim * esz
-    meta_row = 2 * w.head_dim * (esz if w.policy == "topk" else 4)
+    meta_row = 2 * w.head_dim * (esz if w.policy != "gauss" else 4)
     bytes_meta = pages * w.num_kv_heads * meta_row + pages * 4
     bytes_k = int(up.sum()) * page_bytes
     bytes_v = int(vr.sum()) * w.head_dim * esz

@@ -63,7 +63,9 @@ typedef enum { EKV_F32 = 0, EKV_BF16 = 1 } ekv_dtype;
 
 typedef enum {
     EKV_SELECT_TOPK = 0,   /* top-k pages by the bounding-box bound [EntmaxKV §2.B.1] */
-    EKV_SELECT_GAUSS = 1   /* Gaussian-aware tau-hat threshold      [EntmaxKV §2.B.2] */
+    EKV_SELECT_GAUSS = 1,  /* Gaussian-aware tau-hat threshold      [EntmaxKV §2.B.2] */
+    EKV_SELECT_TOPK_SHARED = 2  /* top-k shared by a kv head's query group: one page set
+                                   per kv head, ranked by the group's largest bound */
 } ekv_policy;
 
 /* A paged KV cache.  All pointers are device pointers; the struct itself is
@@ -110,6 +112,7 @@ int entmaxkv_build_page_meta(const ekv_paged_kv* kv, int32_t first_page,
  *       (m_p, s_p) = (scale q.mean_p, scale sqrt(sum_j q_j^2 var_pj)), the mean
  *       and standard deviation of the page's scores under independent
  *       coordinates (needs meta->mean/var).
+ *   EKV_SELECT_TOPK_SHARED: the same per-head bounds as EKV_SELECT_TOPK.
  * Entries past a sequence's last page are not written.  scale must be > 0. */
 int entmaxkv_score_pages(const float* q, int32_t num_q_heads, float scale,
                          const ekv_paged_kv* kv, const ekv_page_meta* meta,
@@ -129,6 +132,11 @@ int entmaxkv_score_pages(const float* q, int32_t num_q_heads, float scale,
  *       cap_pages pages with the largest zmax (ties to the lower page); none ->
  *       the argmax page.  aux (nullable) = (tau-hat, pages passing the
  *       threshold before the cap).
+ *   EKV_SELECT_TOPK_SHARED: one page set per (sequence, kv head), written to
+ *       every query head of its group: the min(cap_pages, NP_b) pages with the
+ *       largest S_p = max over the group's heads of U_p, ties to the lower
+ *       page; aux = (smallest kept S_p, largest S_p not kept or -inf) for each
+ *       head of the group.
  * workspace/ws_bytes are unused (pass NULL, 0). */
 int entmaxkv_select(const float* page_scores, const ekv_paged_kv* kv,
                     int32_t num_q_heads, int32_t policy, int32_t budget_tokens,

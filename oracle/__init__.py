@@ -131,6 +131,25 @@ def select_topk(kv: KV, bound: np.ndarray, kp: int, heads=None):
     return sel, n_sel, kth, nxt
 
 
+def select_topk_shared(kv: KV, bound: np.ndarray, kp: int, heads=None):
+    """Top-k shared by a kv head's query group (one page set per kv head): a
+    page's score for the group is the largest of its G query heads' bounds
+    ([EntmaxKV §2.A] bound, [EntmaxKV §2.B.1] top-k on that score), and every
+    head of the group receives the group's top-kp pages, ties to the lower
+    page.  `bound` must hold every head of the groups named in `heads`.
+    Returns (sel, n_sel, kth, next, shared score) per head."""
+    bound = _f64(bound)
+    G = kv.Hq // kv.meta_shape[1]
+    BH, M = bound.shape
+    h = np.arange(BH) if heads is None else np.asarray(heads)
+    groups = np.unique(h // G)
+    shared = np.full_like(bound, np.nan)
+    for grp in groups:
+        shared[grp * G:(grp + 1) * G] = bound[grp * G:(grp + 1) * G].max(axis=0)
+    sel, n_sel, kth, nxt = select_topk(kv, shared, kp, heads)
+    return sel, n_sel, kth, nxt, shared
+
+
 def score_gauss(kv: KV, meta: Meta, scale: float, heads=None):
     h, nh = _heads(heads)
     m = np.full((kv.BH, kv.pt.shape[1]), np.nan)
@@ -244,6 +263,13 @@ def sparse_step(kv: KV, w, heads=None, meta: Meta | None = None):
         bound = score_bbox(kv, meta, scale, heads)
         sel, n_sel, kth, nxt = select_topk(kv, bound, w.cap_pages, heads)
         res.update(bound=bound, kth=kth, next=nxt)
+    elif w.policy == "topk_shared":
+        G = w.group
+        hh = None if heads is None else np.unique(
+            (np.asarray(heads)[:, None] // G * G + np.arange(G)[None, :]).ravel()).astype(np.int32)
+        bound = score_bbox(kv, meta, scale, hh)
+        sel, n_sel, kth, nxt, shared = select_topk_shared(kv, bound, w.cap_pages, heads)
+        res.update(bound=bound, kth=kth, next=nxt, shared=shared)
     else:
         m, s = score_gauss(kv, meta, scale, heads)
         sel, n_sel, tau_hat, zmax = select_gauss(kv, m, s, w.alpha, w.delta, w.cap_pages, heads)

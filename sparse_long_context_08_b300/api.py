@@ -34,7 +34,8 @@ class EntmaxKVDecoder:
         self.Hq = int(num_q_heads)
         self.scale = float(scale)
         self.alpha = float(alpha)
-        self.policy = E.EKV_SELECT_GAUSS if policy == "gauss" else E.EKV_SELECT_TOPK
+        self.policy = {"topk": E.EKV_SELECT_TOPK, "gauss": E.EKV_SELECT_GAUSS,
+                       "topk_shared": E.EKV_SELECT_TOPK_SHARED}[policy]
         self.budget = int(budget_tokens)
         self.delta = float(delta)
         self.cap = self.budget // kv.page_size

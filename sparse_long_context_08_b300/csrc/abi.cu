@@ -101,9 +101,10 @@ int entmaxkv_score_pages(const float* q, int32_t num_q_heads, float scale,
     if ((st = check_heads(kv, num_q_heads))) return st;
     if (!q || !meta || !page_scores) return EKV_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return EKV_INVALID_ARG;
-    if (policy == EKV_SELECT_TOPK) {
+    if (policy == EKV_SELECT_TOPK || policy == EKV_SELECT_TOPK_SHARED) {
         if (!meta->kmin || !meta->kmax || !aligned16(meta->kmin) || !aligned16(meta->kmax))
             return EKV_INVALID_ARG;
+        policy = EKV_SELECT_TOPK;          // the same per-head bounds
     } else if (policy == EKV_SELECT_GAUSS) {
         if (!meta->mean || !meta->var || !aligned16(meta->mean) || !aligned16(meta->var))
             return EKV_INVALID_ARG;
@@ -128,10 +129,10 @@ int entmaxkv_select(const float* page_scores, const ekv_paged_kv* kv, int32_t nu
     const int cap = budget_tokens / kv->page_size;
     if (budget_tokens <= 0 || cap < 1) return EKV_INVALID_ARG;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (policy == EKV_SELECT_TOPK) {
+    if (policy == EKV_SELECT_TOPK || policy == EKV_SELECT_TOPK_SHARED) {
         if (kv->max_pages > ekv::kMaxPagesTopk) return EKV_UNSUPPORTED;
         return from_cuda(ekv::launch_select_topk(page_scores, to_kv(kv), num_q_heads, cap, sel,
-                                                 n_sel, aux, s));
+                                                 n_sel, aux, policy == EKV_SELECT_TOPK_SHARED, s));
     }
     if (policy == EKV_SELECT_GAUSS) {
         if (!is_alpha(alpha) || !std::isfinite(delta)) return EKV_INVALID_ARG;

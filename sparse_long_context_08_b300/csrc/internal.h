@@ -47,7 +47,7 @@ cudaError_t launch_score(const float* q, int Hq, float scale, const KV& kv, cons
                          const void* kmax, const float* mean, const float* var, int policy,
                          float* out, cudaStream_t s);
 cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp, int32_t* sel,
-                               int32_t* n_sel, float* aux, cudaStream_t s);
+                               int32_t* n_sel, float* aux, bool shared, cudaStream_t s);
 cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, float alpha,
                                 float delta, int32_t* sel, int32_t* n_sel, float* aux,
                                 cudaStream_t s);

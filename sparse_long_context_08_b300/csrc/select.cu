@@ -123,10 +123,14 @@ __device__ int compact_topk(const uint32_t* keys, int n, uint32_t kth, int take_
 // boundary bin is taken whole.  Ties at the k-th key go to the lower pages.
 constexpr int kTopkMaxThreads = 1024;
 
+//
+// Shared (gs > 0, the group size): one CTA per (sequence, kv head) ranks the
+// pages by the largest bound over the group's gs query heads and gives every
+// head of the group that one page set (one page set per kv head).
 __global__ void __launch_bounds__(kTopkMaxThreads)
 select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
                    int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
-                   float* __restrict__ aux) {
+                   float* __restrict__ aux, int gs) {
     pdl_enter();
     extern __shared__ __align__(16) uint32_t keys[];   // [max_pages]
     __shared__ int hist[256];
@@ -135,16 +139,17 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     __shared__ int s_digit, s_above;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nt = blockDim.x, nwarps = nt >> 5;
-    const int bh = blockIdx.x;
+    const int ng = gs > 0 ? gs : 1;       // heads that receive this CTA's selection
+    const int bh = gs > 0 ? (blockIdx.x / kv.hkv) * Hq + (blockIdx.x % kv.hkv) * gs : blockIdx.x;
     const int b = bh / Hq;
     const int np = min(kv.maxp, (kv.sl[b] + kv.P - 1) / kv.P);
     const float* src = bound + (int64_t)bh * kv.maxp;
     int32_t* dst = sel + (int64_t)bh * kp;
     const int k = min(kp, np);
     if (k <= 0) {
-        if (tid == 0) {
-            n_sel[bh] = 0;
-            if (aux) { aux[2 * bh] = INFINITY; aux[2 * bh + 1] = -INFINITY; }
+        if (tid < ng) {
+            n_sel[bh + tid] = 0;
+            if (aux) { aux[2 * (bh + tid)] = INFINITY; aux[2 * (bh + tid) + 1] = -INFINITY; }
         }
         return;
     }
@@ -155,6 +160,13 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
         for (int j = 0; j < 16; ++j) {
             const int i = base + j * nt + tid;
             v[j] = i < np ? __ldcg(src + i) : 0.f;
+        }
+        for (int g = 1; g < ng; ++g) {     // shared: the group's largest bound
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int i = base + j * nt + tid;
+                if (i < np) v[j] = fmaxf(v[j], __ldcg(src + (int64_t)g * kv.maxp + i));
+            }
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -285,10 +297,19 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
             tmin = min(tmin, umin_red[w]);
             nmax = max(nmax, umax_red[w]);
         }
-        n_sel[bh] = k;
-        if (aux) {
-            aux[2 * bh] = key_float(tmin);
-            aux[2 * bh + 1] = any ? key_float(nmax) : -INFINITY;
+        for (int g = 0; g < ng; ++g) {
+            n_sel[bh + g] = k;
+            if (aux) {
+                aux[2 * (bh + g)] = key_float(tmin);
+                aux[2 * (bh + g) + 1] = any ? key_float(nmax) : -INFINITY;
+            }
+        }
+    }
+    if (ng > 1) {                          // the other heads of the group get the same rows
+        __syncthreads();                   // this block's writes of row 0 are visible
+        for (int x = tid; x < (ng - 1) * k; x += nt) {
+            const int g = 1 + x / k, r = x - (g - 1) * k;
+            dst[(int64_t)g * kp + r] = dst[r];
         }
     }
 }
@@ -428,15 +449,18 @@ static int max_optin_smem() {
 }
 
 cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp, int32_t* sel,
-                               int32_t* n_sel, float* aux, cudaStream_t s) {
-    const int threads = kv.maxp <= 8192 ? 256 : (kv.maxp <= 16384 ? 512 : 1024);
+                               int32_t* n_sel, float* aux, bool shared, cudaStream_t s) {
+    // shared: one CTA per (sequence, kv head), G times fewer CTAs, so each
+    // gets the most threads
+    const int threads = shared ? 1024 : (kv.maxp <= 8192 ? 256 : (kv.maxp <= 16384 ? 512 : 1024));
     const size_t smem = (size_t)kv.maxp * 4;
     if ((int)smem > max_optin_smem() - 4096) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(select_topk_kernel, dim3(kv.B * Hq), dim3(threads), smem, s, bound, kv, Hq,
-                      kp, sel, n_sel, aux);
+    const int gs = shared ? Hq / kv.hkv : 0;
+    return launch_pdl(select_topk_kernel, dim3(shared ? kv.B * kv.hkv : kv.B * Hq), dim3(threads),
+                      smem, s, bound, kv, Hq, kp, sel, n_sel, aux, gs);
 }
 
 cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, float alpha,

@@ -26,6 +26,7 @@ EKV_F32 = 0
 EKV_BF16 = 1
 EKV_SELECT_TOPK = 0
 EKV_SELECT_GAUSS = 1
+EKV_SELECT_TOPK_SHARED = 2
 
 SYMBOLS = ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select",
            "entmaxkv_decode", "entmaxkv_workspace_size", "entmaxkv_status_string",

@@ -91,7 +91,7 @@ class Workload:
     dtype: str                 # "f32" or "bf16"
     scale: np.float32          # score scale s (z = s * q.k)
     alpha: float
-    policy: str                # "topk" or "gauss"
+    policy: str                # "topk", "gauss" or "topk_shared"
     budget_tokens: int
     delta: float
     seq_lens: np.ndarray       # int32 [B]

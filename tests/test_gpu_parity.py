@@ -36,12 +36,23 @@ def full_parity(w, heads=None, check_e2e=True):
     hs = list(range(BH)) if heads is None else list(heads)
     s = float(w.scale)
     rep = {}
-    if w.policy == "topk":
-        ob = oracle.score_bbox(kv, om, s, heads=hs)
-        mag = bbox_scale(w, om, hs)
-        compare_scores(w, r["page_scores"], ob, mag, hs)
-        osel, on, okth, onext = oracle.select_topk(kv, ob, w.cap_pages, heads=hs)
-        rep["ties"] = compare_selection(w, r["sel"], r["n_sel"], osel, on, ob, mag, okth, hs)
+    if w.policy in ("topk", "topk_shared"):
+        G = w.group
+        # the shared score needs the bounds of every head of each sampled group
+        hb = hs if w.policy == "topk" else sorted({bh // G * G + g for bh in hs for g in range(G)})
+        ob = oracle.score_bbox(kv, om, s, heads=hb)
+        mag = bbox_scale(w, om, hb)
+        compare_scores(w, r["page_scores"], ob, mag, hb)
+        if w.policy == "topk":
+            osel, on, okth, onext = oracle.select_topk(kv, ob, w.cap_pages, heads=hs)
+            score = ob
+        else:
+            osel, on, okth, onext, score = oracle.select_topk_shared(kv, ob, w.cap_pages, heads=hs)
+            mag = mag.reshape(-1, G, mag.shape[1]).max(axis=1).repeat(G, axis=0)
+            for bh in hs:                       # one page set per kv head
+                g0 = bh // G * G
+                assert np.array_equal(r["sel"][bh, :r["n_sel"][bh]], r["sel"][g0, :r["n_sel"][g0]])
+        rep["ties"] = compare_selection(w, r["sel"], r["n_sel"], osel, on, score, mag, okth, hs)
         for bh in hs:
             assert r["n_sel"][bh] == on[bh]
             if on[bh] < w.pages_of(bh // w.num_q_heads):
@@ -102,6 +113,17 @@ def test_long128k_reduced(alpha):
     full_parity(make_workload("long128k", batch=2, seq_lens=[16384, 12345], alpha=alpha))
 
 
+@pytest.mark.parametrize("over", [
+    {"batch": 2, "seq_lens": [16384, 12345]},
+    {"batch": 2, "seq_lens": [16384, 12345], "alpha": 2.0, "num_q_heads": 16, "num_kv_heads": 2},
+    {"batch": 3, "seq_lens": [5 * 32, 20, 1], "budget_tokens": 4096, "planted_pages": 0},
+])
+def test_shared_selection_reduced(over):
+    """GQA-shared selection: one page set per kv head, ranked by the group's
+    largest bound; decode unchanged."""
+    full_parity(make_workload("long128k", policy="topk_shared", **over))
+
+
 def test_ctx1m_reduced():
     full_parity(make_workload("ctx1m", context=65536))
 
@@ -124,10 +146,11 @@ def sampled_heads(w, n, seed=11):
     return sorted(rng.choice(BH, size=min(n, BH), replace=False).tolist())
 
 
-@pytest.mark.parametrize("name,alpha", [("tiny", 1.5), ("gqa32k", 1.5), ("long128k", 1.5),
-                                        ("long128k", 2.0), ("ctx1m", 1.5), ("gauss64k", 1.5)])
-def test_full_size_sampled_heads(name, alpha):
-    w = make_workload(name, alpha=alpha)
+@pytest.mark.parametrize("name,alpha,policy", [
+    ("tiny", 1.5, None), ("gqa32k", 1.5, None), ("long128k", 1.5, None), ("long128k", 2.0, None),
+    ("ctx1m", 1.5, None), ("gauss64k", 1.5, None), ("long128k", 1.5, "topk_shared")])
+def test_full_size_sampled_heads(name, alpha, policy):
+    w = make_workload(name, alpha=alpha, **({"policy": policy} if policy else {}))
     full_parity(w, heads=sampled_heads(w, 64))
     torch.cuda.empty_cache()
 

@@ -209,6 +209,50 @@ def test_topk_tie_storm_keeps_lowest_pages(oracle_lib):
     assert list(sel[0]) == list(range(7))
 
 
+def test_shared_topk_brute_force_and_group_rows(oracle_lib):
+    """GQA-shared selection: brute force over the pages with the group's
+    largest bound as the score; every head of a group gets the same rows."""
+    rng = np.random.default_rng(11)
+    w = make_workload("gqa32k", num_q_heads=8, num_kv_heads=2, head_dim=8, page_size=4,
+                      batch=2, seq_lens=[4 * 37, 4 * 6 + 1], seed=3)
+    kv = oracle.KV(w)
+    bound = np.round(rng.standard_normal((kv.BH, w.max_pages)) * 2) / 2   # many ties
+    kp, G = 9, 4
+    sel, n_sel, kth, nxt, shared = oracle.select_topk_shared(kv, bound, kp)
+    for bh in range(kv.BH):
+        b, h = divmod(bh, w.num_q_heads)
+        np_ = w.pages_of(b)
+        g0 = b * w.num_q_heads + (h // G) * G
+        score = [max(bound[g0 + g, p] for g in range(G)) for p in range(np_)]   # by hand
+        order = sorted(range(np_), key=lambda p: (-score[p], p))
+        k = min(kp, np_)
+        assert n_sel[bh] == k
+        assert list(sel[bh, :k]) == sorted(order[:k])
+        assert kth[bh] == score[order[k - 1]]
+        assert nxt[bh] == (score[order[kp]] if kp < np_ else -np.inf)
+        assert list(sel[bh, :k]) == list(sel[g0, :k])          # the group's one page set
+    # a planted mistake -- the mean instead of the max over the group -- changes a set
+    wrong = bound.reshape(-1, G, w.max_pages).mean(axis=1).repeat(G, axis=0)
+    s2, n2, _, _ = oracle.select_topk(kv, wrong, kp)
+    assert any(list(s2[bh, :n2[bh]]) != list(sel[bh, :n_sel[bh]]) for bh in range(kv.BH))
+
+
+def test_shared_topk_reduces_to_per_head_topk(oracle_lib):
+    """With one query head per kv head (G = 1), or with every head of a group
+    holding the same bounds, the shared selection is the per-head top-k."""
+    rng = np.random.default_rng(5)
+    w1 = make_workload("gqa32k", num_q_heads=4, num_kv_heads=4, head_dim=8, page_size=4,
+                       batch=2, seq_lens=[4 * 20, 4 * 7], seed=4)
+    kv1 = oracle.KV(w1)
+    b1 = rng.standard_normal((kv1.BH, w1.max_pages))
+    assert np.array_equal(oracle.select_topk_shared(kv1, b1, 6)[0], oracle.select_topk(kv1, b1, 6)[0])
+    w4 = make_workload("gqa32k", num_q_heads=8, num_kv_heads=2, head_dim=8, page_size=4,
+                       batch=2, seq_lens=[4 * 20, 4 * 7], seed=4)
+    kv4 = oracle.KV(w4)
+    b4 = np.repeat(rng.standard_normal((kv4.BH // 4, w4.max_pages)), 4, axis=0)
+    assert np.array_equal(oracle.select_topk_shared(kv4, b4, 6)[0], oracle.select_topk(kv4, b4, 6)[0])
+
+
 # --------------------------------------------------------------------------
 # alpha-entmax threshold
 # --------------------------------------------------------------------------

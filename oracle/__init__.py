@@ -222,6 +222,27 @@ def decode_sparse(kv: KV, scale: float, alpha: float, sel, n_sel, heads=None):
     return out, tau, sup, psum
 
 
+def decode_softmax(kv: KV, scale: float, sel=None, n_sel=None, full: bool = False, heads=None):
+    """Softmax attention over the selected pages (every page when full).
+    Returns (out, lse, outside): outside = the full softmax's mass outside the
+    kept pages when both full and sel are given (NaN otherwise)."""
+    h, nh = _heads(heads)
+    cap = 0
+    if sel is not None:
+        sel = np.ascontiguousarray(sel, dtype=np.int32)
+        n_sel = np.ascontiguousarray(n_sel, dtype=np.int32)
+        cap = sel.shape[1]
+    d = kv.meta_shape[2]
+    out = np.full((kv.BH, d), np.nan)
+    lse = np.full(kv.BH, np.nan)
+    outside = np.full(kv.BH, np.nan)
+    _check(lib().oracle_decode_softmax(kv.ref, _ptr(kv.q), C.c_int(kv.Hq), C.c_double(scale),
+                                       _ptr(sel), _ptr(n_sel), C.c_int(cap), C.c_int(int(full)),
+                                       _ptr(h), C.c_int(nh), _ptr(out), _ptr(lse),
+                                       _ptr(outside)), "decode_softmax")
+    return out, lse, outside
+
+
 @dataclass
 class Full:
     out: np.ndarray

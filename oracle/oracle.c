@@ -482,6 +482,74 @@ int oracle_decode_sparse(const oracle_kv* kv, const float* q, int num_q_heads,
     return bad ? ORACLE_BAD_ARG : ORACLE_OK;
 }
 
+/* Softmax attention, the comparison method of [EntmaxKV] §1 and §4 (a softmax
+ * whose dense tail is truncated to the kept pages).  Scores z = scale q.k over
+ * the valid tokens of the selected pages, or of the whole sequence when full
+ * is set; m = max z, out = sum_i e^(z_i - m) v_i / sum_i e^(z_i - m) and
+ * lse = m + log sum_i e^(z_i - m).  With full set and a selection given,
+ * outside = the full softmax's mass on tokens not in the kept pages. */
+int oracle_decode_softmax(const oracle_kv* kv, const float* q, int num_q_heads,
+                          double scale, const int32_t* sel, const int32_t* n_sel,
+                          int cap, int full, const int32_t* heads, int n_heads,
+                          double* out, double* lse, double* outside) {
+    if (num_q_heads % kv->num_kv_heads || (!full && !sel)) return ORACLE_BAD_ARG;
+    int G = num_q_heads / kv->num_kv_heads;
+    int d = kv->head_dim;
+    int nh = head_count(kv, num_q_heads, heads, n_heads);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic) reduction(|:bad)
+    for (int i = 0; i < nh; ++i) {
+        int bh = head_at(heads, i);
+        int b = bh / num_q_heads, h = bh % num_q_heads, kvh = h / G;
+        const float* qv = q + (int64_t)bh * d;
+        int np = pages_of(kv, b);
+        char* kept = (char*)calloc(np > 0 ? np : 1, 1);
+        if (sel)
+            for (int r = 0; r < n_sel[bh]; ++r) {
+                int p = sel[(int64_t)bh * cap + r];
+                if (p < 0 || p >= np) { bad = 1; continue; }
+                kept[p] = 1;
+            }
+        /* every token attended to (all pages when full, else the kept ones) */
+        int n = 0;
+        for (int p = 0; p < np; ++p)
+            if (full || kept[p]) n += valid_tokens(kv, b, p);
+        double* z = (double*)malloc(sizeof(double) * (n > 0 ? n : 1));
+        int* tb = (int*)malloc(sizeof(int) * (n > 0 ? n : 1));
+        int* tt = (int*)malloc(sizeof(int) * (n > 0 ? n : 1));
+        char* in = (char*)malloc(n > 0 ? n : 1);
+        int k = 0;
+        for (int p = 0; p < np; ++p) {
+            if (!full && !kept[p]) continue;
+            int blk = kv->page_table[(int64_t)b * kv->max_pages + p];
+            for (int t = 0; t < valid_tokens(kv, b, p); ++t) {
+                z[k] = shifted_score(kv, qv, scale, 2.0, blk, kvh, t);   /* (2-1) scale q.k */
+                tb[k] = blk;
+                tt[k] = t;
+                in[k] = kept[p];
+                ++k;
+            }
+        }
+        double* o = out + (int64_t)bh * d;
+        for (int j = 0; j < d; ++j) o[j] = 0.0;
+        double m = -INFINITY, l = 0.0, lin = 0.0;
+        for (int r = 0; r < n; ++r) m = z[r] > m ? z[r] : m;
+        for (int r = 0; r < n; ++r) {
+            double w = exp(z[r] - m);
+            l += w;
+            if (in[r]) lin += w;
+            for (int j = 0; j < d; ++j)
+                o[j] += w * oracle_widen(kv->v_pool, kv->dtype, kv_index(kv, tb[r], kvh, tt[r], j));
+        }
+        if (n > 0)
+            for (int j = 0; j < d; ++j) o[j] /= l;
+        if (lse) lse[bh] = n > 0 ? m + log(l) : -INFINITY;
+        if (outside) outside[bh] = (full && sel && n > 0) ? (l - lin) / l : NAN;
+        free(z); free(tb); free(tt); free(in); free(kept);
+    }
+    return bad ? ORACLE_BAD_ARG : ORACLE_OK;
+}
+
 int oracle_decode_full(const oracle_kv* kv, const float* q, int num_q_heads,
                        double scale, double alpha, const int32_t* sel,
                        const int32_t* n_sel, int cap, const int32_t* heads,

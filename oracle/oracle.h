@@ -118,6 +118,15 @@ int oracle_decode_sparse(const oracle_kv* kv, const float* q, int num_q_heads,
                          int n_heads, double* out, double* tau, int32_t* support,
                          double* psum);
 
+/* Softmax attention over the selected pages' valid tokens (every valid token
+ * when full): out = sum_i e^(z_i - m) v_i / sum_i e^(z_i - m), z = scale q.k,
+ * lse = log sum_i e^(z_i).  full with sel: outside = the full softmax's mass
+ * outside the kept pages (NaN otherwise).  No tokens: out = 0, lse = -inf. */
+int oracle_decode_softmax(const oracle_kv* kv, const float* q, int num_q_heads,
+                          double scale, const int32_t* sel, const int32_t* n_sel,
+                          int cap, int full, const int32_t* heads, int n_heads,
+                          double* out, double* lse, double* outside);
+
 /* Full-cache alpha-entmax attention over every valid token, plus, when sel is
  * given, [EntmaxKV §3] quantities for that kept set: delta = full-cache mass of
  * tokens outside it, covered = (support within it).  vnorm = max_i ||v_i||_2;

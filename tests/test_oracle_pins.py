@@ -254,6 +254,98 @@ def test_shared_topk_reduces_to_per_head_topk(oracle_lib):
 
 
 # --------------------------------------------------------------------------
+# softmax attention (the comparison method)
+# --------------------------------------------------------------------------
+
+def _gather(w, b, kvh, pages):
+    """Keys and values of the valid tokens of `pages` of sequence b, by hand."""
+    K = w.k_pool.astype(np.float64) if w.dtype != "bf16" else bf16_bits_to_f32(w.k_pool).astype(np.float64)
+    V = w.v_pool.astype(np.float64) if w.dtype != "bf16" else bf16_bits_to_f32(w.v_pool).astype(np.float64)
+    ks, vs = [], []
+    for p in pages:
+        blk = w.page_table[b, p]
+        nt = min(w.page_size, w.seq_lens[b] - p * w.page_size)
+        ks.append(K[blk, kvh, :nt]); vs.append(V[blk, kvh, :nt])
+    return np.concatenate(ks), np.concatenate(vs)
+
+
+def test_softmax_decode_brute_force_sparse_and_full(oracle_lib):
+    w = make_workload("gqa32k", num_q_heads=4, num_kv_heads=2, head_dim=16, page_size=4,
+                      batch=2, seq_lens=[4 * 11 + 3, 4 * 5], seed=9)
+    kv = oracle.KV(w)
+    rng = np.random.default_rng(2)
+    cap = 4
+    sel = np.full((kv.BH, cap), -1, np.int32)
+    n_sel = np.zeros(kv.BH, np.int32)
+    for bh in range(kv.BH):
+        np_ = w.pages_of(bh // w.num_q_heads)
+        k = min(cap, np_ - 1)
+        sel[bh, :k] = np.sort(rng.choice(np_, size=k, replace=False))
+        n_sel[bh] = k
+    s = float(w.scale)
+    out, lse, _ = oracle.decode_softmax(kv, s, sel, n_sel)
+    fout, flse, outside = oracle.decode_softmax(kv, s, sel, n_sel, full=True)
+    for bh in range(kv.BH):
+        b, h = divmod(bh, w.num_q_heads)
+        kvh = h // (w.num_q_heads // w.num_kv_heads)
+        qv = w.q[b, h].astype(np.float64)
+        for pages, o, l in [(sel[bh, :n_sel[bh]], out[bh], lse[bh]),
+                            (range(w.pages_of(b)), fout[bh], flse[bh])]:
+            Kt, Vt = _gather(w, b, kvh, pages)
+            z = s * (Kt @ qv)
+            e = np.exp(z - z.max())
+            np.testing.assert_allclose(o, (e @ Vt) / e.sum(), rtol=1e-12, atol=1e-12)
+            assert abs(l - (z.max() + np.log(e.sum()))) < 1e-12
+        # the full softmax's mass outside the kept pages, from the two partition functions
+        assert abs(outside[bh] - (1.0 - np.exp(lse[bh] - flse[bh]))) < 1e-12
+
+
+def test_softmax_decode_constant_keys_is_the_mean_value(oracle_lib):
+    w = make_workload("gqa32k", num_q_heads=2, num_kv_heads=1, head_dim=8, page_size=4,
+                      batch=1, seq_lens=[4 * 6 - 1], seed=1)
+    w.k_pool[:] = w.k_pool[0, 0, 0]
+    kv = oracle.KV(w)
+    out, lse, _ = oracle.decode_softmax(kv, float(w.scale), full=True)
+    _, Vt = _gather(w, 0, 0, range(6))
+    for h in range(2):
+        np.testing.assert_allclose(out[h], Vt.mean(axis=0), rtol=1e-12, atol=1e-12)
+    Kt, _ = _gather(w, 0, 0, [0])
+    z0 = float(w.scale) * Kt[0] @ w.q[0, 0].astype(np.float64)
+    assert abs(lse[0] - (z0 + np.log(23))) < 1e-10
+
+
+def test_entmax_decode_tends_to_softmax_decode(oracle_lib):
+    """alpha -> 1: the (independently pinned) entmax attention approaches the
+    softmax attention over the same kept pages."""
+    w = make_workload("gqa32k", num_q_heads=2, num_kv_heads=1, head_dim=16, page_size=4,
+                      batch=1, seq_lens=[4 * 8], seed=5)
+    kv = oracle.KV(w)
+    sel = np.array([[0, 2, 3, 6]] * 2, np.int32)
+    n_sel = np.array([4, 4], np.int32)
+    so, _, _ = oracle.decode_softmax(kv, float(w.scale), sel, n_sel)
+    errs = []
+    for a in (1.05, 1.01, 1.002):
+        eo, _, _, _ = oracle.decode_sparse(kv, float(w.scale), a, sel, n_sel)
+        errs.append(np.abs(eo - so).max())
+    assert errs[0] > errs[1] > errs[2] and errs[2] < 5e-3, errs
+
+
+def test_softmax_decode_ignores_the_physical_layout(oracle_lib):
+    w = make_workload("gqa32k", num_q_heads=2, num_kv_heads=1, head_dim=8, page_size=4,
+                      batch=1, seq_lens=[4 * 9 - 2], seed=6)
+    kv = oracle.KV(w)
+    a, la, _ = oracle.decode_softmax(kv, float(w.scale), full=True)
+    perm = np.random.default_rng(0).permutation(w.num_blocks)
+    k2, v2 = w.k_pool.copy(), w.v_pool.copy()
+    w.k_pool[perm] = k2
+    w.v_pool[perm] = v2
+    w.page_table[:] = perm[w.page_table]
+    b, lb, _ = oracle.decode_softmax(oracle.KV(w), float(w.scale), full=True)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(la, lb, rtol=1e-13)
+
+
+# --------------------------------------------------------------------------
 # alpha-entmax threshold
 # --------------------------------------------------------------------------
 

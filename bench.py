@@ -31,6 +31,11 @@ if ROOT not in sys.path:
 
 METRIC = "sparse entmax decode µs/step and achieved HBM GB/s (frac of peak) at 128K ctx"
 FULL_METRIC = "full-cache entmax decode µs/step and achieved HBM GB/s (frac of peak)"
+MODE_METRIC = {
+    "full": FULL_METRIC,
+    "softmax": "sparse softmax decode (same kept pages) µs/step and achieved HBM GB/s",
+    "softmax_full": "full-cache softmax decode µs/step and achieved HBM GB/s (frac of peak)",
+}
 FALLBACK_HBM_GBS = 6400.0
 KERNELS_PER_STEP = 5   # score, select, plan, qk, tpv (threshold + values)
 
@@ -52,8 +57,11 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--mode", choices=["sparse", "full"], default="sparse",
-                    help="sparse: the EntmaxKV step (headline); full: full-cache entmax decode")
+    ap.add_argument("--mode", choices=["sparse", "full", "softmax", "softmax_full"],
+                    default="sparse",
+                    help="sparse: the EntmaxKV step (headline); full: full-cache entmax decode; "
+                         "softmax: softmax over the same kept pages; softmax_full: full-cache "
+                         "softmax")
     return ap.parse_args()
 
 
@@ -215,17 +223,30 @@ def oracle_time_per_step(w, seconds: float, steps: int | None = None):
     return statistics.mean(times), desc, cores, times
 
 
-def oracle_full_time_per_step(w, seconds: float, steps: int = 1):
-    """Times the fp64 oracle's full-cache entmax attention on a bounded sample
+def oracle_full_time_per_step(w, seconds: float, steps: int = 1, mode: str = "full"):
+    """Times the fp64 oracle's version of a variant (full-cache entmax, sparse
+    softmax over the selected pages, full-cache softmax) on a bounded sample
     of query heads; returns (us per full step, sample description, cores)."""
     import numpy as np
     import oracle
     kv = oracle.KV(w)
+    meta = oracle.build_meta(kv) if mode == "softmax" else None   # prefill work, not timed
     BH = w.batch * w.num_q_heads
     cores = oracle.get_threads()
+    s = float(w.scale)
+
+    def run(heads):
+        if mode == "full":
+            oracle.decode_full(kv, s, w.alpha, heads=heads)
+        elif mode == "softmax_full":
+            oracle.decode_softmax(kv, s, full=True, heads=heads)
+        else:
+            r = oracle.sparse_step(kv, w, heads=heads, meta=meta)
+            oracle.decode_softmax(kv, s, r["sel"], r["n_sel"], heads=heads)
+
     n0 = min(BH, cores)
     t0 = time.perf_counter()
-    oracle.decode_full(kv, float(w.scale), w.alpha, heads=np.arange(n0, dtype=np.int32))
+    run(np.arange(n0, dtype=np.int32))
     per_head = max(1e-6, (time.perf_counter() - t0) / n0)        # wall time per head, parallel
     n_heads = int(min(BH, max(n0, seconds / max(1, steps) / per_head)))
     rng = np.random.default_rng(0)
@@ -233,10 +254,13 @@ def oracle_full_time_per_step(w, seconds: float, steps: int = 1):
     for _ in range(steps):
         heads = np.sort(rng.choice(BH, size=n_heads, replace=False)).astype(np.int32)
         t0 = time.perf_counter()
-        oracle.decode_full(kv, float(w.scale), w.alpha, heads=heads)
+        run(heads)
         times.append((time.perf_counter() - t0) * 1e6 * BH / n_heads)
-    desc = (f"{n_heads} of {BH} query heads per step (full-cache scores, exact tau, attention; "
-            f"fp64), {steps} steps, scaled to a full step")
+    what = {"full": "full-cache scores, exact tau, attention",
+            "softmax": "bound scores, top-k, softmax attention over the kept pages",
+            "softmax_full": "full-cache scores, softmax attention"}[mode]
+    desc = (f"{n_heads} of {BH} query heads per step ({what}; fp64), {steps} steps, scaled to a "
+            f"full step" + ("; metadata prebuilt" if mode == "softmax" else ""))
     return statistics.mean(times), desc, cores
 
 
@@ -247,14 +271,16 @@ def run_reference(args):
     from sparse_long_context_08_b300.workloads import make_workload
     w = make_workload(args.workload, **overrides(args))
     budget = 150.0
-    if args.mode == "full":
-        oracle_full_time_per_step(w, budget * 0.1, steps=max(1, min(args.warmup, 3)))
-        us, desc, cores = oracle_full_time_per_step(w, budget, steps=max(1, min(args.steps, 5)))
-        line = {"metric": FULL_METRIC, "impl": "reference", "value": us, "unit": "us/step",
+    if args.mode != "sparse":
+        oracle_full_time_per_step(w, budget * 0.1, steps=max(1, min(args.warmup, 3)),
+                                  mode=args.mode)
+        us, desc, cores = oracle_full_time_per_step(w, budget, steps=max(1, min(args.steps, 5)),
+                                                    mode=args.mode)
+        line = {"metric": MODE_METRIC[args.mode], "impl": "reference", "value": us, "unit": "us/step",
                 "n_gpus": args.gpus, "steps": max(1, min(args.steps, 5)), "warmup": args.warmup,
                 "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": dict(workload_config(w), mode="full-cache"),
+                "config": dict(workload_config(w), mode=args.mode),
                 "cpu_baseline": {"value": us, "unit": "us/step", "cores": cores,
                                  "kind": "oracle", "sample": desc},
                 "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0,
@@ -464,13 +490,15 @@ def run_ours(args):
 
 
 def run_full(args):
-    """Full-cache entmax decode (every valid token): plan -> qk -> tpv over the
-    whole cache, timed like the sparse step."""
+    """The variants, timed like the sparse step: full-cache entmax decode (plan
+    -> qk -> tpv over the whole cache), softmax over the kept pages (score ->
+    select -> plan -> qk -> pv -> merge) and full-cache softmax."""
     import torch
     import torch.distributed as dist
 
     from sparse_long_context_08_b300 import entmaxkv as E
-    from sparse_long_context_08_b300.api import EntmaxKVFullDecoder, upload_workload
+    from sparse_long_context_08_b300.api import (EntmaxKVFullDecoder, EntmaxKVSoftmaxDecoder,
+                                                 upload_workload)
     from sparse_long_context_08_b300.workloads import CONFIGS, make_workload
 
     rank, local_rank, world = dist_env()
@@ -481,7 +509,21 @@ def run_full(args):
     w = make_workload(args.workload, seed=CONFIGS[args.workload]["seed"] + 1000 * rank,
                       **overrides(args))
     kv, q = upload_workload(w)
-    dec = EntmaxKVFullDecoder(kv, w.num_q_heads, float(w.scale), w.alpha)
+    mode = args.mode
+    pre = []                                   # stages before the decode call
+    if mode == "full":
+        dec = EntmaxKVFullDecoder(kv, w.num_q_heads, float(w.scale), w.alpha)
+        step = lambda: dec.decode(q)
+        dnames, launches = ["plan", "qk", "tpv"], 3
+    else:
+        dec = EntmaxKVSoftmaxDecoder(kv, w.num_q_heads, float(w.scale), w.policy, w.budget_tokens,
+                                     w.delta, w.alpha, full=(mode == "softmax_full"))
+        dec.build_meta()
+        step = lambda: dec.step(q)
+        dnames, launches = ["plan", "qk", "pv"], 4
+        if mode == "softmax":
+            pre = [("score", lambda: dec.sparse.score(q)), ("select", lambda: dec.sparse.select())]
+            launches = 6
     torch.cuda.synchronize()
     flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device="cuda")
     flush_read = torch.ones(max(1, args.flush_mb // 2) << 20, dtype=torch.uint8, device="cuda")
@@ -491,7 +533,7 @@ def run_full(args):
         flush_read.sum(dtype=torch.int32)
 
     stream = torch.cuda.current_stream()
-    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4 + len(pre))]
     for x in evs:
         x.record()
     torch.cuda.synchronize()
@@ -499,15 +541,18 @@ def run_full(args):
     cap_stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(cap_stream):
         for _ in range(2):
-            dec.decode(q)
+            step()
     torch.cuda.current_stream().wait_stream(cap_stream)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=cap_stream):
-        dec.decode(q)
+        step()
     staged = torch.cuda.CUDAGraph()
     with torch.cuda.graph(staged, stream=cap_stream):
-        E.entmaxkv_set_stage_events(evs)
+        for j, (_, fn) in enumerate(pre):
+            evs[j].record()
+            fn()
+        E.entmaxkv_set_stage_events(evs[len(pre):])
         dec.decode(q)
         E.entmaxkv_set_stage_events(None)
     torch.cuda.synchronize()
@@ -520,7 +565,7 @@ def run_full(args):
         dist.barrier()
 
     K = args.steps
-    names = ["plan", "qk", "tpv"]
+    names = [n for n, _ in pre] + dnames
     stage = {n: [] for n in names}
     total = []
     t_start = torch.cuda.Event(enable_timing=True)
@@ -549,17 +594,22 @@ def run_full(args):
     ms_per_step = float(t_sum.item()) / K
 
     up, vr = E.entmaxkv_decode_counts(dec.workspace, w.batch, w.num_q_heads, w.num_kv_heads,
-                                      w.head_dim, w.page_size, w.max_pages, w.max_pages)
+                                      w.head_dim, w.page_size, w.max_pages, dec.cap if mode != "full"
+                                      else w.max_pages)
     esz = 2 if w.dtype == "bf16" else 4
     page_bytes = w.page_size * w.head_dim * esz
     bytes_k = int(up.sum()) * page_bytes
-    bytes_v = int(vr.sum()) * w.head_dim * esz
+    # entmax reads the V rows of its support; softmax the V of every page it attends to
+    bytes_v = int(vr.sum()) * w.head_dim * esz if mode == "full" else bytes_k
     small = 2 * w.batch * w.num_q_heads * w.head_dim * 4 + w.batch * w.max_pages * 4
-    bytes_step = bytes_k + bytes_v + small
+    pages = sum(w.pages_of(b) for b in range(w.batch))
+    bytes_meta = pages * w.num_kv_heads * 2 * w.head_dim * esz if mode == "softmax" else 0
+    bytes_step = bytes_meta + bytes_k + bytes_v + small
     mean = {n: statistics.mean(v) for n, v in stage.items()}
     dom = max(mean, key=mean.get)
     peak, peak_kind = measured_peak()
-    dom_bytes = {"qk": bytes_k, "tpv": bytes_v}.get(dom)
+    dom_bytes = {"score": bytes_meta or None, "qk": bytes_k,
+                 "tpv": bytes_v, "pv": bytes_v}.get(dom)
     achieved = dom_bytes / (mean[dom] * 1e-3) / 1e9 if dom_bytes else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
@@ -587,11 +637,11 @@ def run_full(args):
             dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
         e2e = {"value": float(t_e2e.item()) / world * 1e6, "unit": "us/step",
                "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4,
-               "timing": "host wall clock per step incl. H2D, the call, D2H and sync"}
+               "timing": "host wall clock per step incl. H2D, the calls, D2H and sync"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        us, desc, cores = oracle_full_time_per_step(w, args.cpu_seconds)
+        us, desc, cores = oracle_full_time_per_step(w, args.cpu_seconds, mode=mode)
         cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc}
 
     if world > 1:
@@ -601,19 +651,20 @@ def run_full(args):
             dist.destroy_process_group()
         return
     line = {
-        "metric": FULL_METRIC, "value": ms_per_step * 1e3 / world, "unit": "us/step",
+        "metric": MODE_METRIC[mode], "value": ms_per_step * 1e3 / world, "unit": "us/step",
         "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic", "config": dict(workload_config(w), mode="full-cache"),
+        "dtype": "f32", "data": "synthetic", "config": dict(workload_config(w), mode=mode),
         "hbm_gbs": bytes_step / (ms_per_step * 1e-3) / 1e9,
         "hbm_frac_of_measured": bytes_step / (ms_per_step * 1e-3) / 1e9 / peak,
         "bytes_per_step": bytes_step,
-        "bytes_breakdown": {"k_all_pages": bytes_k, "v_support_rows": bytes_v,
+        "bytes_breakdown": {"metadata": bytes_meta, "k_pages": bytes_k,
+                            ("v_support_rows" if mode == "full" else "v_pages"): bytes_v,
                             "q_out_page_table": small, "pages": int(up.sum()),
-                            "v_rows": int(vr.sum())},
+                            "v_rows": int(vr.sum()) if mode == "full" else None},
         "stage_us": {n: v * 1e3 for n, v in mean.items()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 3 * K, "clocks": clocks,
+        "gpu_launches": launches * K, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -624,7 +675,7 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
-    elif args.mode == "full":
+    elif args.mode != "sparse":
         run_full(args)
     else:
         run_ours(args)

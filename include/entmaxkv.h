@@ -183,6 +183,36 @@ size_t entmaxkv_full_workspace_size(int32_t batch, int32_t num_q_heads,
                                     int32_t num_kv_heads, int32_t head_dim,
                                     int32_t page_size, int32_t max_pages);
 
+/* Softmax attention over the selected pages: the comparison method of
+ * [EntmaxKV] §1 and §4 (a softmax whose dense tail is truncated to the kept
+ * pages), computed by the same plan and score kernels as entmaxkv_decode.
+ * For each (b, h): z = scale q.k over the valid tokens of pages sel[b, h,
+ * 0:n_sel[b, h]] (as entmaxkv_decode), out = sum_i e^(z_i - m) v_i /
+ * sum_i e^(z_i - m) with m = max z, and lse_out (nullable) fp32 [batch,
+ * num_q_heads] = log sum_i e^(z_i).  Every selected token has a positive weight,
+ * so the V rows of all selected pages are read (each kv head's union once).
+ * An empty selection gives out = 0, lse = -inf.  workspace: at least
+ * entmaxkv_softmax_workspace_size(...) bytes, 256-byte aligned, not shared
+ * with a concurrent call.  Errors as entmaxkv_decode. */
+int entmaxkv_decode_softmax(const float* q, int32_t num_q_heads, float scale,
+                            const ekv_paged_kv* kv, const int32_t* sel,
+                            const int32_t* n_sel, int32_t cap_pages, float* out,
+                            float* lse_out, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/* Full-cache softmax attention (every valid token): entmaxkv_decode_softmax
+ * without a selection; workspace of entmaxkv_softmax_workspace_size(...,
+ * cap_pages = max_pages) bytes. */
+int entmaxkv_decode_softmax_full(const float* q, int32_t num_q_heads, float scale,
+                                 const ekv_paged_kv* kv, float* out, float* lse_out,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* Host-only: bytes of workspace the softmax decodes need (0 if invalid). */
+size_t entmaxkv_softmax_workspace_size(int32_t batch, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim,
+                                       int32_t page_size, int32_t max_pages,
+                                       int32_t cap_pages);
+
 /* Bytes of the scratch array built into the library for
  * entmaxkv_decode_noalloc. */
 #define ENTMAXKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)

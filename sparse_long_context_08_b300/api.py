@@ -127,3 +127,55 @@ class EntmaxKVFullDecoder:
             q_dev.copy_(q_host, non_blocking=True)
             self.decode(q_dev, s)
             out_host.copy_(self.out, non_blocking=True)
+
+
+class EntmaxKVSoftmaxDecoder:
+    """Softmax attention over the pages the EntmaxKV scoring and selection keep
+    (the comparison method: a softmax whose dense tail is truncated to the kept
+    pages), or over every token with full=True.  The selection stage is the
+    entmax pipeline's own (alpha only matters for the Gaussian tau-hat)."""
+
+    def __init__(self, kv: E.PagedKV, num_q_heads: int, scale: float, policy: str = "topk",
+                 budget_tokens: int = 4096, delta: float = 0.0, alpha: float = 1.5,
+                 full: bool = False):
+        self.kv = kv
+        self.Hq = int(num_q_heads)
+        self.scale = float(scale)
+        self.full = bool(full)
+        dev = kv.k_pool.device
+        B, Hq = kv.batch, self.Hq
+        self.sparse = None if full else EntmaxKVDecoder(kv, num_q_heads, scale, alpha, policy,
+                                                        budget_tokens, delta)
+        self.cap = kv.max_pages if full else self.sparse.cap
+        self.out = torch.empty((B, Hq, kv.head_dim), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        ws = E.entmaxkv_softmax_workspace_size(B, Hq, kv.num_kv_heads, kv.head_dim, kv.page_size,
+                                               kv.max_pages, self.cap)
+        if ws == 0:
+            raise ValueError("invalid sizes for the softmax workspace")
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def build_meta(self, stream=None) -> None:
+        if self.sparse is not None:
+            self.sparse.build_meta(stream=stream)
+
+    def decode(self, q: torch.Tensor, stream=None) -> torch.Tensor:
+        sel = None if self.full else self.sparse.sel
+        n_sel = None if self.full else self.sparse.n_sel
+        E.entmaxkv_decode_softmax(q, self.Hq, self.scale, self.kv, sel, n_sel, self.cap, self.out,
+                                  self.lse, self.workspace, stream)
+        return self.out
+
+    def step(self, q: torch.Tensor, stream=None) -> torch.Tensor:
+        if self.sparse is not None:
+            self.sparse.score(q, stream)
+            self.sparse.select(stream)
+        return self.decode(q, stream)
+
+    def step_host(self, q_host: torch.Tensor, out_host: torch.Tensor, q_dev: torch.Tensor,
+                  stream=None) -> None:
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            q_dev.copy_(q_host, non_blocking=True)
+            self.step(q_dev, s)
+            out_host.copy_(self.out, non_blocking=True)

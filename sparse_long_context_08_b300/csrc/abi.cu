@@ -201,6 +201,54 @@ int entmaxkv_decode_full(const float* q, int32_t num_q_heads, float scale, const
                                              static_cast<cudaStream_t>(stream)));
 }
 
+size_t entmaxkv_softmax_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t page_size, int32_t max_pages,
+                                       int32_t cap_pages) {
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+        head_dim <= 0 || page_size <= 0 || max_pages <= 0 || cap_pages <= 0)
+        return 0;
+    return ekv::softmax_layout(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages,
+                               cap_pages).total;
+}
+
+static int softmax_impl(const float* q, int32_t num_q_heads, float scale, const ekv_paged_kv* kv,
+                        const int32_t* sel, const int32_t* n_sel, int32_t cap_pages, bool full,
+                        float* out, float* lse_out, void* workspace, size_t ws_bytes,
+                        void* stream) {
+    int st = check_kv(kv, true, true);
+    if (st) return st;
+    if ((st = check_heads(kv, num_q_heads))) return st;
+    if (!q || !out || !workspace || (!full && (!sel || !n_sel))) return EKV_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return EKV_INVALID_ARG;
+    if (cap_pages < 1) return EKV_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EKV_INVALID_ARG;
+    if ((int64_t)kv->max_pages > ekv::kMaxPagesTopk) return EKV_UNSUPPORTED;
+    if ((int64_t)kv->num_blocks * kv->num_kv_heads * kv->page_size > INT32_MAX) return EKV_UNSUPPORTED;
+    const ekv::DecodeLayout L = ekv::softmax_layout(kv->batch, num_q_heads, kv->num_kv_heads,
+                                                    kv->head_dim, kv->page_size, kv->max_pages,
+                                                    cap_pages);
+    if (ws_bytes < L.total) return EKV_WORKSPACE_TOO_SMALL;
+    return from_cuda(ekv::launch_decode_softmax(q, num_q_heads, scale, to_kv(kv), sel, n_sel,
+                                                cap_pages, full, out, lse_out, workspace, L,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int entmaxkv_decode_softmax(const float* q, int32_t num_q_heads, float scale,
+                            const ekv_paged_kv* kv, const int32_t* sel, const int32_t* n_sel,
+                            int32_t cap_pages, float* out, float* lse_out, void* workspace,
+                            size_t ws_bytes, void* stream) {
+    return softmax_impl(q, num_q_heads, scale, kv, sel, n_sel, cap_pages, false, out, lse_out,
+                        workspace, ws_bytes, stream);
+}
+
+int entmaxkv_decode_softmax_full(const float* q, int32_t num_q_heads, float scale,
+                                 const ekv_paged_kv* kv, float* out, float* lse_out,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+    if (!kv) return EKV_INVALID_ARG;
+    return softmax_impl(q, num_q_heads, scale, kv, nullptr, nullptr, kv->max_pages, true, out,
+                        lse_out, workspace, ws_bytes, stream);
+}
+
 int entmaxkv_set_stage_events(void* const* events, int32_t n_events) {
     if (n_events != 0 && (n_events != 4 || !events)) return EKV_INVALID_ARG;
     ekv::set_decode_stage_events(reinterpret_cast<const cudaEvent_t*>(events), n_events);

@@ -46,7 +46,8 @@ constexpr int kTpvTile = kTpvThreads * kTpvVec * 4;    // scores per tile
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap) {
+DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap,
+                           bool candidates) {
     (void)D;
     DecodeLayout L{};
     L.U = B * Hkv;
@@ -66,11 +67,21 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, 
     L.tau = take(sizeof(float) * (size_t)B * Hq);
     L.ccap = cap * P;
     L.cand_x = L.cand_pos = 0;
-    if (L.ccap > kTpvSmemCand) {
+    if (candidates && L.ccap > kTpvSmemCand) {
         L.cand_x = take(sizeof(float) * (size_t)B * Hq * L.ccap);
         L.cand_pos = take(sizeof(int) * (size_t)B * Hq * L.ccap);
     }
+    L.recs = 0;
+    L.nrec = 0;
     L.total = o;
+    return L;
+}
+
+DecodeLayout softmax_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap) {
+    DecodeLayout L = decode_layout(B, Hq, Hkv, D, P, max_pages, cap, false);
+    L.nrec = kPvMaxWarps + L.U;
+    L.recs = L.total;
+    L.total = align256(L.recs + sizeof(float) * (size_t)L.nrec * L.G * (D + 1));
     return L;
 }
 
@@ -1017,6 +1028,281 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
 }
 
 // ---------------------------------------------------------------------------
+// softmax attention over the union pages (the comparison method)
+//
+// pv_softmax: the flattened union lists are cut into one contiguous range per
+// warp, as for qk; each warp streams its V pages through a private ring of
+// bulk copies and, per page, forms the weights e^(z - m_h) of the G heads (z
+// from qk, m_h the head's max) and accumulates sum_t w v_t (lane: D / 32
+// dimensions of every head) and sum_t w.  A warp flushes one partial record
+// per segment of its range inside one unit: segments that start a unit go to
+// slot kPvMaxWarps + u, a segment that starts the warp's range inside a unit
+// to slot `warp`.  softmax_merge recomputes the segment starts of each unit
+// and adds its records in order, so the result does not depend on timing.
+// ---------------------------------------------------------------------------
+constexpr int kPvWarps = 4;
+constexpr int kPvCtasPerSm = 2;
+constexpr int kPvStageBytes = 24 * 1024;
+
+template <typename T, int DPL>
+__device__ __forceinline__ void load_dpl(const unsigned char* p, float (&x)[DPL]) {
+    if constexpr (sizeof(T) == 4) {
+        if constexpr (DPL == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(p);
+            x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+        } else {
+            const float2 f = *reinterpret_cast<const float2*>(p);
+            x[0] = f.x; x[1] = f.y;
+        }
+    } else {
+        if constexpr (DPL == 4) {
+            const uint2 r = *reinterpret_cast<const uint2*>(p);
+            x[0] = __uint_as_float(r.x << 16); x[1] = __uint_as_float(r.x & 0xFFFF0000u);
+            x[2] = __uint_as_float(r.y << 16); x[3] = __uint_as_float(r.y & 0xFFFF0000u);
+        } else {
+            const uint32_t r = *reinterpret_cast<const uint32_t*>(p);
+            x[0] = __uint_as_float(r << 16); x[1] = __uint_as_float(r & 0xFFFF0000u);
+        }
+    }
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kPvWarps * 32, kPvCtasPerSm)
+pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
+    pdl_enter();
+    constexpr int DPL = D / 32;
+    constexpr int NW = (32 * G + 31) / 32;        // weights per lane per page (P <= 32)
+    extern __shared__ __align__(128) unsigned char s_pv[];
+    __shared__ int red[40];
+    __shared__ __align__(8) uint64_t s_bar[kPvWarps][8];
+    __shared__ __align__(16) float s_w[kPvWarps][32 * G];     // [token][head]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = kv.P;
+    const uint32_t page_bytes = static_cast<uint32_t>(P * D * sizeof(T));
+    unsigned char* ring = s_pv + (size_t)warp * ns * page_bytes;
+    int* s_prefix = reinterpret_cast<int*>(s_pv + (size_t)kPvWarps * ns * page_bytes);
+    uint64_t* bar = s_bar[warp];
+    {
+        const int U = L.U;
+        const int seg = (U + blockDim.x - 1) / blockDim.x;
+        const int a0 = min(U, tid * seg), a1 = min(U, a0 + seg);
+        int c = 0;
+        for (int a = a0; a < a1; ++a) c += __ldcg(ws.union_count + a);
+        int tot;
+        int run = block_exclusive_scan(c, red, &tot);
+        for (int a = a0; a < a1; ++a) {
+            s_prefix[a] = run;
+            run += __ldcg(ws.union_count + a);
+        }
+        if (tid == 0) s_prefix[U] = tot;
+    }
+    if (lane == 0) {
+        for (int st = 0; st < ns; ++st) mbar_init(&bar[st], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int total = s_prefix[L.U];
+    const int64_t nwg = (int64_t)gridDim.x * kPvWarps;
+    const int wg = blockIdx.x * kPvWarps + warp;
+    const int f0 = (int)((int64_t)total * wg / nwg);
+    const int f1 = (int)((int64_t)total * (wg + 1) / nwg);
+    const int npg = f1 - f0;
+    if (npg <= 0) return;
+    const unsigned char* vbase = static_cast<const unsigned char*>(kv.v);
+    const uint64_t evict_first = l2_evict_first_policy();
+
+    PgDesc cur = resolve_page(f0 + lane, f1, s_prefix, kv, ws, L);
+    PgDesc nxt{-1, 0, 0, 0, 0};
+    if (npg > 32) nxt = resolve_page(f0 + 32 + lane, f1, s_prefix, kv, ws, L);
+    int cur_base = 0;
+    auto issue = [&](int k) -> PgDesc {
+        PgDesc dsc{-1, 0, 0, 0, 0};
+        if (k >= npg) return dsc;
+        if (k >= cur_base + 32) {
+            cur = nxt;
+            cur_base += 32;
+            if (npg > cur_base + 32) nxt = resolve_page(f0 + cur_base + 32 + lane, f1, s_prefix, kv, ws, L);
+        }
+        dsc = shfl_desc(cur, k - cur_base);
+        if (lane == 0) {
+            const int st = k % ns;
+            if (dsc.blk >= 0) {
+                mbar_arrive_expect_tx(&bar[st], page_bytes);
+                bulk_g2s_hint(ring + (size_t)st * page_bytes,
+                              vbase + ((int64_t)dsc.blk * kv.hkv + dsc.u % kv.hkv) * page_bytes,
+                              page_bytes, &bar[st], evict_first);
+            } else {
+                mbar_arrive(&bar[st]);
+            }
+        }
+        return dsc;
+    };
+
+    float acc[G][DPL];
+    float lsum[NW];               // this lane's share of sum_t w for head (lane + 32 j) / 32 ... see below
+    float mh[G];
+    int cur_u = -1, slot = -1;
+    auto flush = [&]() {
+        float* rec = ws.recs + (int64_t)slot * G * (D + 1);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) rec[g * D + lane * DPL + e] = acc[g][e];
+        // weight index x = lane + 32 j covers head x / 32 (token x % 32)
+#pragma unroll
+        for (int j = 0; j < NW; ++j) {
+            const float l = warp_sum(lsum[j]);
+            if (lane == 0 && j < G) rec[G * D + j] = l;
+        }
+    };
+    PgDesc dq[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+        if (x < ns - 1) dq[x] = issue(x);
+    bool failed = false;
+    for (int k = 0; k < npg; ++k) {
+        const int st = k % ns;
+        {
+            const PgDesc nd = issue(k + ns - 1);
+            const int nst = (k + ns - 1) % ns;
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                if (x == nst) dq[x] = nd;
+        }
+        PgDesc d{};
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+            if (x == st) d = dq[x];
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[st], (uint32_t)((k / ns) & 1)))) {
+            failed = true;
+            break;
+        }
+        if (d.u != cur_u) {
+            if (cur_u >= 0) flush();
+            cur_u = d.u;
+            slot = (f0 + k == s_prefix[d.u]) ? kPvMaxWarps + d.u : wg;
+            const int b = cur_u / kv.hkv, kvh = cur_u - b * kv.hkv;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint32_t key = __ldcg(ws.head_max + b * Hq + kvh * G + g);
+                mh[g] = key == 0u ? 0.f : key_float(key);      // no score: every weight is 0
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[g][e] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < NW; ++j) lsum[j] = 0.f;
+        }
+        // weights of the page: entry x = lane + 32 j is head x / 32, token x % 32
+        const float* zrow = ws.z + ((int64_t)d.u * G) * L.Umax * P + (int64_t)d.i * P;
+#pragma unroll
+        for (int j = 0; j < NW; ++j) {
+            const int g = j, t = lane;
+            float w = 0.f;
+            if (g < G && t < P && t < d.valid && ((d.mask >> g) & 1)) {
+                const float z = __ldcg(zrow + (int64_t)g * L.Umax * P + t);
+                w = __expf(z - mh[g]);
+            }
+            if (g < G && t < P) s_w[warp][t * G + g] = w;
+            lsum[j] += w;
+        }
+        __syncwarp();
+        const unsigned char* pg = ring + (size_t)st * page_bytes + (size_t)lane * DPL * sizeof(T);
+        const int nt = d.blk >= 0 ? d.valid : 0;
+        for (int t = 0; t < nt; ++t) {
+            float v[DPL];
+            load_dpl<T, DPL>(pg + (size_t)t * D * sizeof(T), v);
+            const float* wt = &s_w[warp][t * G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float w = wt[g];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[g][e] = fmaf(w, v[e], acc[g][e]);
+            }
+        }
+        __syncwarp();        // every lane is done with stage st and s_w before they are refilled
+    }
+    if (failed) {
+        if (lane == 0) flag_bad_data();
+        return;
+    }
+    if (cur_u >= 0) flush();
+}
+
+// out = sum of the unit's records / sum of their weights; lse = m + log(l).
+__global__ void __launch_bounds__(128)
+softmax_merge_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int nwg, float* __restrict__ out,
+                     float* __restrict__ lse_out) {
+    pdl_enter();
+    __shared__ int red[40];
+    __shared__ int s_w[1024];
+    __shared__ int s_n;
+    const int G = L.G, D = kv.D;
+    const int bh = blockIdx.x;
+    const int b = bh / Hq, h = bh - b * Hq;
+    const int kvh = h / G, g = h - kvh * G;
+    const int u = b * kv.hkv + kvh;
+    const int tid = threadIdx.x;
+    // a = pages of the units before u, e = a + count_u, total = all pages
+    int ca = 0, ct = 0;
+    for (int x = tid; x < L.U; x += blockDim.x) {
+        const int c = __ldcg(ws.union_count + x);
+        ct += c;
+        if (x < u) ca += c;
+    }
+    const int a = block_sum_i(ca, red);
+    const int total = block_sum_i(ct, red);
+    const int cnt = __ldcg(ws.union_count + u);
+    const int e = a + cnt;
+    // warps whose range starts strictly inside [a, e) and is not empty, ascending
+    if (tid == 0) s_n = 0;
+    __syncthreads();
+    if (cnt > 0 && total > 0) {
+        const int w_lo = (int)(((int64_t)a * nwg) / total);
+        const int w_hi = min(nwg - 1, (int)(((int64_t)e * nwg) / total) + 1);
+        for (int w = w_lo + tid; w <= w_hi; w += blockDim.x) {
+            const int fw = (int)((int64_t)total * w / nwg);
+            const int fn = (int)((int64_t)total * (w + 1) / nwg);
+            if (fw > a && fw < e && fn > fw) {
+                const int at = atomicAdd(&s_n, 1);
+                if (at < 1024) s_w[at] = w;
+            }
+        }
+    }
+    __syncthreads();
+    const int n = min(s_n, 1024);
+    if (s_n > 1024 && tid == 0) flag_bad_data();
+    // ascending warp order (n is small): one thread sorts
+    if (tid == 0)
+        for (int i = 1; i < n; ++i) {
+            const int v = s_w[i];
+            int j = i - 1;
+            while (j >= 0 && s_w[j] > v) { s_w[j + 1] = s_w[j]; --j; }
+            s_w[j + 1] = v;
+        }
+    __syncthreads();
+    float l = 0.f;
+    if (cnt > 0) {
+        const float* r0 = ws.recs + (int64_t)(kPvMaxWarps + u) * G * (D + 1);
+        l = __ldcg(r0 + G * D + g);
+        for (int i = 0; i < n; ++i)
+            l += __ldcg(ws.recs + (int64_t)s_w[i] * G * (D + 1) + G * D + g);
+    }
+    for (int dd = tid; dd < D; dd += blockDim.x) {
+        float o = 0.f;
+        if (cnt > 0) {
+            o = __ldcg(ws.recs + (int64_t)(kPvMaxWarps + u) * G * (D + 1) + g * D + dd);
+            for (int i = 0; i < n; ++i)
+                o += __ldcg(ws.recs + (int64_t)s_w[i] * G * (D + 1) + g * D + dd);
+        }
+        out[(int64_t)bh * D + dd] = l > 0.f ? o / l : 0.f;
+    }
+    if (tid == 0 && lse_out) {
+        const uint32_t key = __ldcg(ws.head_max + bh);
+        lse_out[bh] = (l > 0.f && key != 0u) ? key_float(key) + logf(l) : -INFINITY;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
 static cudaEvent_t g_stage_events[4];
@@ -1094,11 +1380,10 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
     return cudaSuccess;
 }
 
-// qk and tpv after a plan: scores of the union pages, then threshold and values.
+// qk after a plan: z = qscale q.k of the union pages, and each head's max.
 template <typename T, int D, int G>
-static cudaError_t launch_qk_tpv(const float* q, int Hq, float scale, const KV& kv, int cap,
-                                 float alpha, float* out, float* tau_out, int32_t* support_out,
-                                 const WS& ws, const DecodeLayout& L, cudaStream_t s) {
+static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv, const WS& ws,
+                             const DecodeLayout& L, cudaStream_t s) {
     cudaError_t e;
     if constexpr (sizeof(T) == 2) {
         const int page_bytes = kv.P * D * 2;
@@ -1109,7 +1394,7 @@ static cudaError_t launch_qk_tpv(const float* q, int Hq, float scale, const KV& 
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
         e = launch_pdl(qk_mma_kernel<D, G>, dim3(sm_count() * kQmCtasPerSm), dim3(kQmWarps * 32),
-                       smem, s, q, Hq, (alpha - 1.f) * scale, kv, ws, L, ns);
+                       smem, s, q, Hq, qscale, kv, ws, L, ns);
         if (e != cudaSuccess) return e;
     } else {
         const size_t page_bytes = (size_t)kv.P * D * sizeof(T);
@@ -1123,9 +1408,19 @@ static cudaError_t launch_qk_tpv(const float* q, int Hq, float scale, const KV& 
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
         e = launch_pdl(qk_kernel<T, D, G>, dim3(sm_count()), dim3(kQkThreads), smem, s, q, Hq,
-                       (alpha - 1.f) * scale, kv, ws, L, ns, std::min(kQkGroup, ns));
+                       qscale, kv, ws, L, ns, std::min(kQkGroup, ns));
         if (e != cudaSuccess) return e;
     }
+    return cudaSuccess;
+}
+
+// qk and tpv after a plan: scores of the union pages, then threshold and values.
+template <typename T, int D, int G>
+static cudaError_t launch_qk_tpv(const float* q, int Hq, float scale, const KV& kv, int cap,
+                                 float alpha, float* out, float* tau_out, int32_t* support_out,
+                                 const WS& ws, const DecodeLayout& L, cudaStream_t s) {
+    cudaError_t e = launch_qk<T, D, G>(q, Hq, (alpha - 1.f) * scale, kv, ws, L, s);
+    if (e != cudaSuccess) return e;
     const int E = fabsf(alpha - 1.5f) < 1e-6f ? 2 : (fabsf(alpha - 2.f) < 1e-6f ? 1 : 0);
     if (E == 2) return launch_tpv<2, T, D>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
     if (E == 1) return launch_tpv<1, T, D>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
@@ -1173,6 +1468,60 @@ cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, con
     EKV_DISPATCH_T(kv.dtype, EKV_DISPATCH_D(kv.D, EKV_DISPATCH_G(G, {
         return launch_decode_t<T, kD, kG>(q, Hq, scale, kv, sel, n_sel, cap, alpha, out, tau_out,
                                            support_out, ws, L, s);
+    })))
+    return cudaErrorInvalidValue;
+}
+
+template <typename T, int D, int G>
+static cudaError_t launch_decode_softmax_t(const float* q, int Hq, float scale, const KV& kv,
+                                           const int32_t* sel, const int32_t* n_sel, int cap,
+                                           bool full, float* out, float* lse_out, const WS& ws,
+                                           const DecodeLayout& L, cudaStream_t s) {
+    cudaError_t e;
+    if (L.U > kMaxUnits || !ws.recs) return cudaErrorInvalidValue;
+    stage_mark(0, s);
+    if (full) {
+        if (L.Umax != kv.maxp) return cudaErrorInvalidValue;
+        const int chunks = (kv.maxp + kPlanAllChunk - 1) / kPlanAllChunk;
+        e = launch_pdl(plan_all_kernel, dim3(L.U, chunks), dim3(kPlanThreads), 0, s, kv, Hq, ws, L);
+    } else {
+        if (cap > kPlanSelRegs * kPlanThreads / G) return cudaErrorInvalidValue;
+        const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax);
+        e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel,
+                       cap, ws, L);
+    }
+    if (e != cudaSuccess) return e;
+    e = launch_qk<T, D, G>(q, Hq, scale, kv, ws, L, s);
+    if (e != cudaSuccess) return e;
+    const int page_bytes = kv.P * D * (int)sizeof(T);
+    const int ns = std::max(2, std::min(8, kPvStageBytes / page_bytes));   // 16 KiB fp32 pages: 2
+    const int grid = std::min(sm_count() * kPvCtasPerSm, kPvMaxWarps / kPvWarps);
+    const size_t smem = (size_t)kPvWarps * ns * page_bytes + (size_t)(L.U + 1) * sizeof(int);
+    e = cudaFuncSetAttribute(pv_softmax_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    stage_mark(2, s);
+    e = launch_pdl(pv_softmax_kernel<T, D, G>, dim3(grid), dim3(kPvWarps * 32), smem, s, Hq, kv, ws,
+                   L, ns);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(softmax_merge_kernel, dim3(kv.B * Hq), dim3(128), 0, s, Hq, kv, ws, L,
+                   grid * kPvWarps, out, lse_out);
+    if (e != cudaSuccess) return e;
+    stage_mark(3, s);
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_softmax(const float* q, int Hq, float scale, const KV& kv,
+                                  const int32_t* sel, const int32_t* n_sel, int cap, bool full,
+                                  float* out, float* lse_out, void* ws_base, const DecodeLayout& L,
+                                  cudaStream_t s) {
+    const WS ws = ws_views(ws_base, L);
+    const int G = L.G;
+    EKV_DISPATCH_T(kv.dtype, EKV_DISPATCH_D(kv.D, EKV_DISPATCH_G(G, {
+        return launch_decode_softmax_t<T, kD, kG>(q, Hq, scale, kv, sel, n_sel, cap, full, out,
+                                                   lse_out, ws, L, s);
     })))
     return cudaErrorInvalidValue;
 }

@@ -32,13 +32,19 @@ struct KV {
 // head's selection (cap * P tokens) is larger than the threshold kernel keeps
 // in shared memory, the candidates go to per-head global buffers of ccap =
 // cap * P entries (cand_x, cand_pos; absent otherwise).
+//
+// The softmax decode adds partial-sum records (recs, nrec slots of G * (D + 1)
+// floats): one slot per streaming warp plus one per unit.
 struct DecodeLayout {
-    int    U, G, Umax, nvw, ccap;
+    int    U, G, Umax, nvw, ccap, nrec;
     size_t union_count, head_max, union_page, union_mask, union_blk, vtok, vrows;
-    size_t z, tau, cand_x, cand_pos, total;
+    size_t z, tau, cand_x, cand_pos, recs, total;
 };
 constexpr int kTpvSmemCand = 16384;      // candidates per head the shared-memory threshold kernel holds
-DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap);
+constexpr int kPvMaxWarps = 4096;        // streaming-warp record slots of the softmax decode
+DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap,
+                           bool candidates = true);
+DecodeLayout softmax_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, int cap);
 
 cudaError_t launch_build_meta(const KV& kv, int first_page, int num_pages, void* kmin,
                               void* kmax, float* mean, float* var, bool bbox, bool gauss,
@@ -54,6 +60,13 @@ cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, 
 cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, const int32_t* sel,
                           const int32_t* n_sel, int cap, float alpha, float* out, float* tau_out,
                           int32_t* support_out, void* ws, const DecodeLayout& L, cudaStream_t s);
+// Softmax attention over the selected pages (full: every page), laid out by
+// softmax_layout; lse_out (nullable) receives log sum_i e^(z_i).
+cudaError_t launch_decode_softmax(const float* q, int Hq, float scale, const KV& kv,
+                                  const int32_t* sel, const int32_t* n_sel, int cap, bool full,
+                                  float* out, float* lse_out, void* ws, const DecodeLayout& L,
+                                  cudaStream_t s);
+
 // Full-cache decode: every valid token of every sequence, for all heads
 // (workspace laid out by decode_layout(..., cap = max_pages)).
 cudaError_t launch_decode_full(const float* q, int Hq, float scale, const KV& kv, float alpha,

@@ -23,6 +23,7 @@ struct WS {
     float* tau;
     float* cand_x;        // [B * Hq][ccap] candidates, then weights (large selections only)
     int* cand_pos;        // [B * Hq][ccap] their score index, then V row
+    float* recs;          // [nrec][G][D + 1] softmax partial sums (softmax decode only)
 };
 inline WS ws_views(void* base, const DecodeLayout& L) {
     char* c = static_cast<char*>(base);
@@ -32,7 +33,8 @@ inline WS ws_views(void* base, const DecodeLayout& L) {
               reinterpret_cast<int*>(c + L.vrows), reinterpret_cast<float*>(c + L.z),
               reinterpret_cast<float*>(c + L.tau),
               L.cand_x ? reinterpret_cast<float*>(c + L.cand_x) : nullptr,
-              L.cand_pos ? reinterpret_cast<int*>(c + L.cand_pos) : nullptr};
+              L.cand_pos ? reinterpret_cast<int*>(c + L.cand_pos) : nullptr,
+              L.recs ? reinterpret_cast<float*>(c + L.recs) : nullptr};
 }
 
 __device__ __forceinline__ int pages_of(const KV& kv, int b) {

@@ -32,7 +32,8 @@ SYMBOLS = ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select"
            "entmaxkv_decode", "entmaxkv_workspace_size", "entmaxkv_status_string",
            "entmaxkv_read_device_status", "entmaxkv_version", "entmaxkv_set_stage_events",
            "entmaxkv_decode_counts", "entmaxkv_decode_noalloc", "entmaxkv_decode_full",
-           "entmaxkv_full_workspace_size")
+           "entmaxkv_full_workspace_size", "entmaxkv_decode_softmax",
+           "entmaxkv_decode_softmax_full", "entmaxkv_softmax_workspace_size")
 
 
 class EntmaxKVError(RuntimeError):
@@ -81,10 +82,15 @@ def lib() -> C.CDLL:
         L.entmaxkv_decode_full.argtypes = [vp, i32, f32, vp, f32, vp, vp, vp, vp, sz, vp]
         L.entmaxkv_full_workspace_size.argtypes = [i32] * 6
         L.entmaxkv_full_workspace_size.restype = sz
+        L.entmaxkv_decode_softmax.argtypes = [vp, i32, f32, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+        L.entmaxkv_decode_softmax_full.argtypes = [vp, i32, f32, vp, vp, vp, vp, sz, vp]
+        L.entmaxkv_softmax_workspace_size.argtypes = [i32] * 7
+        L.entmaxkv_softmax_workspace_size.restype = sz
         for name in ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select",
                      "entmaxkv_decode", "entmaxkv_read_device_status",
                      "entmaxkv_set_stage_events", "entmaxkv_decode_counts", "entmaxkv_decode_noalloc",
-                     "entmaxkv_decode_full"):
+                     "entmaxkv_decode_full", "entmaxkv_decode_softmax",
+                     "entmaxkv_decode_softmax_full"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -308,6 +314,36 @@ def entmaxkv_decode_full(q: torch.Tensor, num_q_heads: int, scale: float, kv: Pa
            lib().entmaxkv_decode_full(_ptr(q), num_q_heads, float(scale), kv.ref, float(alpha),
                                       _ptr(out), _ptr(tau_out), _ptr(support_out),
                                       _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def entmaxkv_softmax_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                                    max_pages, cap_pages) -> int:
+    return int(lib().entmaxkv_softmax_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                     page_size, max_pages, cap_pages))
+
+
+def entmaxkv_decode_softmax(q: torch.Tensor, num_q_heads: int, scale: float, kv: PagedKV,
+                            sel: torch.Tensor | None, n_sel: torch.Tensor | None, cap_pages: int,
+                            out: torch.Tensor, lse_out: torch.Tensor | None,
+                            workspace: torch.Tensor, stream=None) -> None:
+    """Softmax attention over the selected pages (sel None: every page)."""
+    _need(q, "q", torch.float32, (kv.batch, num_q_heads, kv.head_dim))
+    _need(out, "out", torch.float32, (kv.batch, num_q_heads, kv.head_dim))
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, (kv.batch, num_q_heads))
+    _need(workspace, "workspace", torch.uint8)
+    if sel is None:
+        _check("entmaxkv_decode_softmax_full",
+               lib().entmaxkv_decode_softmax_full(_ptr(q), num_q_heads, float(scale), kv.ref,
+                                                  _ptr(out), _ptr(lse_out), _ptr(workspace),
+                                                  workspace.numel(), _stream(stream)))
+        return
+    _need(sel, "sel", torch.int32, (kv.batch, num_q_heads, cap_pages))
+    _need(n_sel, "n_sel", torch.int32, (kv.batch, num_q_heads))
+    _check("entmaxkv_decode_softmax",
+           lib().entmaxkv_decode_softmax(_ptr(q), num_q_heads, float(scale), kv.ref, _ptr(sel),
+                                         _ptr(n_sel), cap_pages, _ptr(out), _ptr(lse_out),
+                                         _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def entmaxkv_read_device_status(stream=None) -> int:

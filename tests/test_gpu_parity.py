@@ -208,6 +208,68 @@ def test_large_selection_uses_global_candidates():
 
 
 # ---------------------------------------------------------------------------
+# softmax attention (the comparison method) against the oracle's softmax
+# ---------------------------------------------------------------------------
+
+LSE_TOL = 1e-5
+
+
+def softmax_parity(w, heads=None, full=False):
+    from sparse_long_context_08_b300.api import EntmaxKVSoftmaxDecoder, upload_workload
+    kv_d, q = upload_workload(w)
+    dec = EntmaxKVSoftmaxDecoder(kv_d, w.num_q_heads, float(w.scale), w.policy, w.budget_tokens,
+                                 w.delta, w.alpha, full=full)
+    dec.build_meta()
+    BH = w.batch * w.num_q_heads
+    hs = list(range(BH)) if heads is None else list(heads)
+    kv = oracle.KV(w)
+    if full:
+        dec.decode(q)
+        o_out, o_lse, _ = oracle.decode_softmax(kv, float(w.scale), full=True, heads=hs)
+    else:
+        dec.step(q)            # the GPU's own selection feeds the GPU decode ...
+        torch.cuda.synchronize()
+        sel = dec.sparse.sel.cpu().numpy().reshape(BH, -1)
+        n_sel = dec.sparse.n_sel.cpu().numpy().reshape(BH)
+        # ... and the oracle attends to the same pages
+        o_out, o_lse, _ = oracle.decode_softmax(kv, float(w.scale), sel, n_sel, heads=hs)
+    torch.cuda.synchronize()
+    out = dec.out.cpu().numpy().astype(np.float64).reshape(BH, -1)
+    lse = dec.lse.cpu().numpy().astype(np.float64).reshape(BH)
+    for bh in hs:
+        if np.isinf(o_lse[bh]):
+            assert np.isinf(lse[bh]) and np.all(out[bh] == 0)
+            continue
+        assert abs(lse[bh] - o_lse[bh]) <= LSE_TOL * max(1.0, abs(o_lse[bh])), (bh, lse[bh], o_lse[bh])
+        err = np.abs(out[bh] - o_out[bh])
+        ok = err <= 1e-4 + 2e-3 * np.abs(o_out[bh])
+        assert ok.all(), (bh, err.max())
+    assert E.entmaxkv_read_device_status() == E.EKV_OK
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", {}),
+    ("gqa32k", {"batch": 2, "seq_lens": [8192, 5000]}),
+    ("long128k", {"batch": 2, "seq_lens": [16384, 12345]}),
+    ("long128k", {"batch": 2, "seq_lens": [3000, 2049], "num_q_heads": 8, "num_kv_heads": 1,
+                  "page_size": 16, "budget_tokens": 512, "head_dim": 64}),
+    ("long128k", {"batch": 2, "seq_lens": [3000, 2049], "num_q_heads": 8, "num_kv_heads": 8,
+                  "dtype": "f32", "budget_tokens": 512}),
+    ("gauss64k", {"batch": 2, "seq_lens": [16384, 9999]}),
+])
+@pytest.mark.parametrize("full", [False, True])
+def test_softmax_decode(name, over, full):
+    softmax_parity(make_workload(name, **over), full=full)
+
+
+@pytest.mark.parametrize("full", [False, True])
+def test_softmax_decode_full_size_sampled_heads(full):
+    w = make_workload("long128k")
+    softmax_parity(w, heads=sampled_heads(w, 48), full=full)
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
 # shapes: head_dim, dtype, group size, page size, general alpha
 # ---------------------------------------------------------------------------
 

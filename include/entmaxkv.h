@@ -213,6 +213,18 @@ size_t entmaxkv_softmax_workspace_size(int32_t batch, int32_t num_q_heads,
                                        int32_t page_size, int32_t max_pages,
                                        int32_t cap_pages);
 
+/* Measurement aid [EntmaxKV §3]: after an entmaxkv_decode that used
+ * `workspace` (same sizes), mass_out[b, h] (device fp32) = sum over the valid
+ * tokens of the kept pages of ((alpha-1) z_i - tau[b, h])_+^(1/(alpha-1)), the
+ * weight an alpha-entmax with threshold tau (device fp32 [batch, num_q_heads],
+ * e.g. the full-cache tau_out of entmaxkv_decode_full) puts on the kept
+ * tokens; 1 - mass_out is that distribution's mass outside the kept pages
+ * (delta in the page's error bound).  Asynchronous on `stream`. */
+int entmaxkv_kept_mass(void* workspace, int32_t batch, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                       int32_t max_pages, int32_t cap_pages, float alpha,
+                       const float* tau, float* mass_out, void* stream);
+
 /* Bytes of the scratch array built into the library for
  * entmaxkv_decode_noalloc. */
 #define ENTMAXKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)

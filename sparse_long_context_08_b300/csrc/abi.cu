@@ -268,6 +268,20 @@ int entmaxkv_decode_counts(void* workspace, int32_t batch, int32_t num_q_heads,
                                              static_cast<cudaStream_t>(stream)));
 }
 
+int entmaxkv_kept_mass(void* workspace, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t page_size, int32_t max_pages, int32_t cap_pages,
+                       float alpha, const float* tau, float* mass_out, void* stream) {
+    if (!workspace || !tau || !mass_out || !is_alpha(alpha)) return EKV_INVALID_ARG;
+    if (entmaxkv_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages,
+                                cap_pages) == 0)
+        return EKV_INVALID_ARG;
+    const ekv::DecodeLayout L = ekv::decode_layout(batch, num_q_heads, num_kv_heads, head_dim,
+                                                   page_size, max_pages, cap_pages);
+    return from_cuda(ekv::launch_kept_mass(num_q_heads, alpha, page_size, workspace, L, tau,
+                                           mass_out, batch * num_q_heads,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 int entmaxkv_read_device_status(int32_t* status_out, void* stream) {
     if (!status_out) return EKV_INVALID_ARG;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);

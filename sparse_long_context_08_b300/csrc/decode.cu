@@ -1303,6 +1303,41 @@ softmax_merge_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int nwg, float* __res
 }
 
 // ---------------------------------------------------------------------------
+// kept mass: sum over a head's kept tokens of (z' - tau)_+^(1/(alpha-1)) for a
+// given threshold tau (e.g. the full-cache one), from the scores a sparse
+// decode left in its workspace.  One CTA per head.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+kept_mass_kernel(int Hq, float alpha, int P, WS ws, DecodeLayout L, const float* __restrict__ tau,
+                 float* __restrict__ mass) {
+    __shared__ float red[40];
+    const int G = L.G;
+    const int bh = blockIdx.x;
+    const int b = bh / Hq, h = bh - b * Hq;
+    const int kvh = h / G, hg = h - kvh * G;
+    const int u = b * (Hq / G) + kvh;
+    const int n = __ldcg(ws.union_count + u) * P;
+    const float* z = ws.z + ((int64_t)u * G + hg) * L.Umax * P;
+    const float t = __ldg(tau + bh);
+    const float ex = 1.f / (alpha - 1.f);
+    const int E = fabsf(alpha - 1.5f) < 1e-6f ? 2 : (fabsf(alpha - 2.f) < 1e-6f ? 1 : 0);
+    float acc = 0.f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const float a = __ldcg(z + i) - t;
+        if (a > 0.f) acc += pow_e(a, E, ex);
+    }
+    acc = block_sum(acc, red);
+    if (threadIdx.x == 0) mass[bh] = acc;
+}
+
+cudaError_t launch_kept_mass(int Hq, float alpha, int P, void* ws_base, const DecodeLayout& L,
+                             const float* tau, float* mass, int BH, cudaStream_t s) {
+    const WS ws = ws_views(ws_base, L);
+    kept_mass_kernel<<<BH, 256, 0, s>>>(Hq, alpha, P, ws, L, tau, mass);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
 static cudaEvent_t g_stage_events[4];

@@ -73,6 +73,11 @@ cudaError_t launch_decode_full(const float* q, int Hq, float scale, const KV& kv
                                float* out, float* tau_out, int32_t* support_out, void* ws,
                                const DecodeLayout& L, cudaStream_t s);
 
+// Mass the alpha-entmax with per-head threshold tau puts on each head's kept
+// tokens, from the scores a decode left in the workspace.
+cudaError_t launch_kept_mass(int Hq, float alpha, int P, void* ws, const DecodeLayout& L,
+                             const float* tau, float* mass, int BH, cudaStream_t s);
+
 // Optional events recorded between the decode kernels (plan | qk | tpv):
 // events[0] before plan, [1] before qk, [2] before tpv, [3] after tpv.
 // n = 0 disables.  Process-wide; for measurement only.

@@ -33,7 +33,8 @@ SYMBOLS = ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select"
            "entmaxkv_read_device_status", "entmaxkv_version", "entmaxkv_set_stage_events",
            "entmaxkv_decode_counts", "entmaxkv_decode_noalloc", "entmaxkv_decode_full",
            "entmaxkv_full_workspace_size", "entmaxkv_decode_softmax",
-           "entmaxkv_decode_softmax_full", "entmaxkv_softmax_workspace_size")
+           "entmaxkv_decode_softmax_full", "entmaxkv_softmax_workspace_size",
+           "entmaxkv_kept_mass")
 
 
 class EntmaxKVError(RuntimeError):
@@ -84,13 +85,14 @@ def lib() -> C.CDLL:
         L.entmaxkv_full_workspace_size.restype = sz
         L.entmaxkv_decode_softmax.argtypes = [vp, i32, f32, vp, vp, vp, i32, vp, vp, vp, sz, vp]
         L.entmaxkv_decode_softmax_full.argtypes = [vp, i32, f32, vp, vp, vp, vp, sz, vp]
+        L.entmaxkv_kept_mass.argtypes = [vp] + [i32] * 7 + [f32, vp, vp, vp]
         L.entmaxkv_softmax_workspace_size.argtypes = [i32] * 7
         L.entmaxkv_softmax_workspace_size.restype = sz
         for name in ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select",
                      "entmaxkv_decode", "entmaxkv_read_device_status",
                      "entmaxkv_set_stage_events", "entmaxkv_decode_counts", "entmaxkv_decode_noalloc",
                      "entmaxkv_decode_full", "entmaxkv_decode_softmax",
-                     "entmaxkv_decode_softmax_full"):
+                     "entmaxkv_decode_softmax_full", "entmaxkv_kept_mass"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -344,6 +346,19 @@ def entmaxkv_decode_softmax(q: torch.Tensor, num_q_heads: int, scale: float, kv:
            lib().entmaxkv_decode_softmax(_ptr(q), num_q_heads, float(scale), kv.ref, _ptr(sel),
                                          _ptr(n_sel), cap_pages, _ptr(out), _ptr(lse_out),
                                          _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def entmaxkv_kept_mass(workspace: torch.Tensor, batch, num_q_heads, num_kv_heads, head_dim,
+                       page_size, max_pages, cap_pages, alpha: float, tau: torch.Tensor,
+                       mass_out: torch.Tensor, stream=None) -> None:
+    """Mass the alpha-entmax with threshold tau puts on each head's kept tokens
+    (after an entmaxkv_decode on `workspace`)."""
+    _need(tau, "tau", torch.float32, (batch, num_q_heads))
+    _need(mass_out, "mass_out", torch.float32, (batch, num_q_heads))
+    _check("entmaxkv_kept_mass",
+           lib().entmaxkv_kept_mass(_ptr(workspace), batch, num_q_heads, num_kv_heads, head_dim,
+                                    page_size, max_pages, cap_pages, float(alpha), _ptr(tau),
+                                    _ptr(mass_out), _stream(stream)))
 
 
 def entmaxkv_read_device_status(stream=None) -> int:

@@ -270,6 +270,48 @@ def test_softmax_decode_full_size_sampled_heads(full):
 
 
 # ---------------------------------------------------------------------------
+# discarded mass of the kept pages: entmax delta and the softmax mass outside
+# ---------------------------------------------------------------------------
+
+def mass_parity(w, heads=None):
+    from sparse_long_context_08_b300.mass import RECOVERED_TOL, measure
+    m = measure(w)
+    BH = w.batch * w.num_q_heads
+    hs = list(range(BH)) if heads is None else list(heads)
+    kv = oracle.KV(w)
+    s = float(w.scale)
+    f = oracle.decode_full(kv, s, w.alpha, m["sel"], m["n_sel"], heads=hs)
+    _, _, outside = oracle.decode_softmax(kv, s, m["sel"], m["n_sel"], full=True, heads=hs)
+    for bh in hs:
+        assert abs(m["delta"][bh] - f.delta[bh]) <= 1e-4, (bh, m["delta"][bh], f.delta[bh])
+        assert abs(m["softmax_outside"][bh] - outside[bh]) <= 5e-4, \
+            (bh, m["softmax_outside"][bh], outside[bh])
+        if f.covered[bh]:
+            assert m["recovered"][bh], (bh, m["delta"][bh])
+        elif f.delta[bh] > 10 * RECOVERED_TOL:
+            assert not m["recovered"][bh], (bh, m["delta"][bh], f.delta[bh])
+    return m
+
+
+@pytest.mark.parametrize("name,over", [
+    ("gqa32k", {"batch": 2, "seq_lens": [8192, 5000]}),
+    ("long128k", {"batch": 2, "seq_lens": [16384, 12345]}),
+    ("long128k", {"batch": 2, "seq_lens": [16384, 12345], "alpha": 2.0}),
+    ("long128k", {"batch": 1, "context": 8192, "alpha": 1.3, "seed": 7}),
+    ("gauss64k", {"batch": 2, "seq_lens": [16384, 9999]}),
+])
+def test_discarded_mass(name, over):
+    m = mass_parity(make_workload(name, **over))
+    assert np.all(m["softmax_outside"] > 0)       # softmax keeps weight on every token
+
+
+def test_discarded_mass_full_size_sampled_heads():
+    w = make_workload("long128k")
+    mass_parity(w, heads=sampled_heads(w, 32))
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
 # shapes: head_dim, dtype, group size, page size, general alpha
 # ---------------------------------------------------------------------------
 

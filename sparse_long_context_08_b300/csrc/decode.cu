@@ -64,12 +64,14 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int D, int P, int max_pages, 
     L.vtok = take(sizeof(uint32_t) * (size_t)L.U * L.nvw);
     L.vrows = take(sizeof(int) * L.U);
     L.z = take(sizeof(float) * (size_t)L.U * L.G * L.Umax * P);
+    L.pmax = take(sizeof(float) * (size_t)L.U * L.G * L.Umax);
     L.tau = take(sizeof(float) * (size_t)B * Hq);
     L.ccap = cap * P;
-    L.cand_x = L.cand_pos = 0;
+    L.cand_x = L.cand_pos = L.plist = 0;
     if (candidates && L.ccap > kTpvSmemCand) {
         L.cand_x = take(sizeof(float) * (size_t)B * Hq * L.ccap);
         L.cand_pos = take(sizeof(int) * (size_t)B * Hq * L.ccap);
+        L.plist = take(sizeof(int) * (size_t)B * Hq * L.Umax);
     }
     L.recs = 0;
     L.nrec = 0;
@@ -183,7 +185,7 @@ struct QkInfo { int u, i, valid, mask; };
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kQkThreads, 1)
 qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, DecodeLayout L,
-          int nslots, int group) {
+          int nslots, int group, int write_pm) {
     pdl_enter();
     using C = QkCfg<T, D, G>;
     extern __shared__ __align__(128) unsigned char s_raw[];
@@ -356,6 +358,12 @@ qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, Decod
             for (int hh = 0; hh < G; ++hh)
                 if (hh == h) hm[hh] = fmaxf(hm[hh], m4);
         }
+        if (write_pm && lane < G) {           // head `lane`'s largest z' on this page
+            float pm = -INFINITY;
+            if ((in.mask >> lane) & 1)
+                for (int t = 0; t < in.valid; ++t) pm = fmaxf(pm, st[lane * P + t]);
+            ws.pmax[((int64_t)in.u * L.Umax + in.i) * G + lane] = pm;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
     }
@@ -419,7 +427,7 @@ __device__ __forceinline__ PgDesc shfl_desc(const PgDesc& d, int src) {
                   __shfl_sync(0xFFFFFFFFu, d.mask, src)};
 }
 
-template <int D, int G>
+template <int D, int G, bool kPM>      // kPM: also write each head's page maxima
 __global__ void __launch_bounds__(kQmWarps * 32, kQmCtasPerSm)
 qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, DecodeLayout L,
               int ns) {
@@ -550,6 +558,7 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
                     }
         }
         const unsigned char* pg = ring + (size_t)st * page_bytes;
+        float pgm = -INFINITY;               // head g's largest z' on this page (this lane's tokens)
         for (int nt = 0; nt < P / 8; ++nt) {
             float c[C::MT][4];
 #pragma unroll
@@ -588,9 +597,15 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
                 z1 = (hin && tok + 1 < d.valid) ? z1 : -INFINITY;
                 *reinterpret_cast<float2*>(ws.z + (((int64_t)d.u * G + g) * L.Umax + d.i) * P + tok) =
                     make_float2(z0, z1);
-                hm = fmaxf(hm, fmaxf(z0, z1));
+                pgm = fmaxf(pgm, fmaxf(z0, z1));
             }
         }
+        if constexpr (kPM) {
+            pgm = fmaxf(pgm, __shfl_xor_sync(0xFFFFFFFFu, pgm, 1));
+            pgm = fmaxf(pgm, __shfl_xor_sync(0xFFFFFFFFu, pgm, 2));
+            if (g < G && t == 0) ws.pmax[((int64_t)d.u * L.Umax + d.i) * G + g] = pgm;
+        }
+        hm = fmaxf(hm, pgm);
         __syncwarp();        // every lane is done with stage st before it is refilled
     }
     if (failed) {
@@ -609,6 +624,40 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
 // ---------------------------------------------------------------------------
 // tpv: exact alpha-entmax threshold and value accumulation, one CTA per head
 // ---------------------------------------------------------------------------
+constexpr int kTpvPmVec = 8;          // page maxima per thread per round trip
+
+// Union pages i < ucnt of a head whose largest z' exceeds max - 1 (only those
+// can hold a token with nonzero weight), written to list[] in a fixed thread
+// order; returns their count.  pm[] holds the first round of maxima (entries
+// j * blockDim + tid); later rounds are read from pmr (page i at pmr[i * G]).
+// Every thread calls it.
+__device__ int list_candidate_pages(float (&pm)[kTpvPmVec], const float* __restrict__ pmr, int G,
+                                    int ucnt, float mx, int* list, int* ired) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    int npl = 0;
+    for (int p0 = 0; p0 < ucnt; p0 += kTpvPmVec * nt) {
+        if (p0 > 0) {
+#pragma unroll
+            for (int j = 0; j < kTpvPmVec; ++j) {
+                const int i = p0 + j * nt + tid;
+                pm[j] = i < ucnt ? __ldcg(pmr + (int64_t)i * G) : -INFINITY;
+            }
+        }
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < kTpvPmVec; ++j) c += (p0 + j * nt + tid < ucnt) && pm[j] - mx > -1.f;
+        int tot;
+        int pos = npl + block_exclusive_scan(c, ired, &tot);
+#pragma unroll
+        for (int j = 0; j < kTpvPmVec; ++j) {
+            const int i = p0 + j * nt + tid;
+            if (i < ucnt && pm[j] - mx > -1.f) list[pos++] = i;
+        }
+        npl += tot;
+    }
+    __syncthreads();
+    return npl;
+}
 __device__ __forceinline__ float pow_e(float a, int E, float ex) {
     return E == 2 ? a * a : (E == 1 ? a : powf(a, ex));
 }
@@ -876,6 +925,13 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
 
     const uint32_t key = __ldcg(ws.head_max + bh);
     const int ucnt = __ldcg(ws.union_count + u);
+    const float* pmr = ws.pmax + (int64_t)u * L.Umax * G + hg;     // stride G
+    float pm[kTpvPmVec];
+#pragma unroll
+    for (int j = 0; j < kTpvPmVec; ++j) {
+        const int i = j * kTpvThreads + tid;
+        pm[j] = i < L.Umax ? __ldcg(pmr + (int64_t)i * G) : -INFINITY;
+    }
     const int n = ucnt * P;
     if (key == 0u || n == 0) {
         for (int i = tid; i < D; i += blockDim.x) outb[i] = 0.f;
@@ -888,24 +944,26 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
     }
     const float mx = key_float(key);
 
-    // candidates x = z' - max > -1, compacted in a fixed thread order
+    // pages that can hold a candidate, then their candidates x = z' - max >
+    // -1, compacted in a fixed thread order
+    int* pl = ws.plist + (int64_t)bh * L.Umax;
+    const int npl = list_candidate_pages(pm, pmr, G, ucnt, mx, pl, ired);   // ends with a barrier
     int m = 0;
-    for (int t0 = 0; t0 < n; t0 += kTpvTile) {
+    const int ne = npl * P;
+    for (int t0 = 0; t0 < ne; t0 += kTpvTile) {
         float v[kTpvVec * 4];
+        int zi[kTpvVec];
 #pragma unroll
         for (int j = 0; j < kTpvVec; ++j) {
-            const int i = t0 + (j * kTpvThreads + tid) * 4;
-            const float4 f = i < n ? __ldcg(reinterpret_cast<const float4*>(z + i))
-                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+            const int e = t0 + (j * kTpvThreads + tid) * 4;
+            zi[j] = e < ne ? __ldcg(pl + e / P) * P + e % P : 0;
+            const float4 f = e < ne ? __ldcg(reinterpret_cast<const float4*>(z + zi[j]))
+                                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            v[4 * j] = f.x - mx; v[4 * j + 1] = f.y - mx; v[4 * j + 2] = f.z - mx; v[4 * j + 3] = f.w - mx;
         }
         int c = 0;
 #pragma unroll
-        for (int j = 0; j < kTpvVec * 4; ++j) {
-            const int i = t0 + ((j >> 2) * kTpvThreads + tid) * 4 + (j & 3);
-            v[j] = i < n ? v[j] - mx : -INFINITY;
-            c += v[j] > -1.f;
-        }
+        for (int j = 0; j < kTpvVec * 4; ++j) c += v[j] > -1.f;
         int tot;
         int pos = m + block_exclusive_scan(c, ired, &tot);
 #pragma unroll
@@ -913,7 +971,7 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
             if (v[j] > -1.f) {
                 if (pos < L.ccap) {
                     cx[pos] = v[j];
-                    cp[pos] = t0 + ((j >> 2) * kTpvThreads + tid) * 4 + (j & 3);
+                    cp[pos] = zi[j >> 2] + (j & 3);
                 }
                 ++pos;
             }
@@ -1395,7 +1453,7 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
     const int cand_cap = cap * kv.P;
     cudaError_t e;
     if (cand_cap > kTpvSmemCand) {
-        if (!ws.cand_x || L.ccap < cand_cap) return cudaErrorInvalidValue;
+        if (!ws.cand_x || !ws.plist || L.ccap < cand_cap) return cudaErrorInvalidValue;
         stage_mark(2, s);
         e = launch_pdl(tpv_global_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvThreads), 0, s, Hq,
                        alpha, kv, ws, L, out, tau_out, support_out);
@@ -1415,21 +1473,23 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
     return cudaSuccess;
 }
 
-// qk after a plan: z = qscale q.k of the union pages, and each head's max.
+// qk after a plan: z = qscale q.k of the union pages, and each head's max;
+// with pm also each head's maximum on every union page.
 template <typename T, int D, int G>
 static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv, const WS& ws,
-                             const DecodeLayout& L, cudaStream_t s) {
+                             const DecodeLayout& L, bool pm, cudaStream_t s) {
     cudaError_t e;
     if constexpr (sizeof(T) == 2) {
         const int page_bytes = kv.P * D * 2;
         const int ns = std::min(8, kQmStageBytes / page_bytes);
         const size_t smem = (size_t)kQmWarps * ns * page_bytes + (size_t)(L.U + 1) * sizeof(int);
         if (ns < 2) return cudaErrorInvalidValue;
-        e = cudaFuncSetAttribute(qk_mma_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        auto kernel = pm ? qk_mma_kernel<D, G, true> : qk_mma_kernel<D, G, false>;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
-        e = launch_pdl(qk_mma_kernel<D, G>, dim3(sm_count() * kQmCtasPerSm), dim3(kQmWarps * 32),
-                       smem, s, q, Hq, qscale, kv, ws, L, ns);
+        e = launch_pdl(kernel, dim3(sm_count() * kQmCtasPerSm), dim3(kQmWarps * 32), smem, s, q, Hq,
+                       qscale, kv, ws, L, ns);
         if (e != cudaSuccess) return e;
     } else {
         const size_t page_bytes = (size_t)kv.P * D * sizeof(T);
@@ -1443,7 +1503,7 @@ static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv,
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
         e = launch_pdl(qk_kernel<T, D, G>, dim3(sm_count()), dim3(kQkThreads), smem, s, q, Hq,
-                       qscale, kv, ws, L, ns, std::min(kQkGroup, ns));
+                       qscale, kv, ws, L, ns, std::min(kQkGroup, ns), pm ? 1 : 0);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -1454,7 +1514,9 @@ template <typename T, int D, int G>
 static cudaError_t launch_qk_tpv(const float* q, int Hq, float scale, const KV& kv, int cap,
                                  float alpha, float* out, float* tau_out, int32_t* support_out,
                                  const WS& ws, const DecodeLayout& L, cudaStream_t s) {
-    cudaError_t e = launch_qk<T, D, G>(q, Hq, (alpha - 1.f) * scale, kv, ws, L, s);
+    // page maxima only where the threshold kernel scans large selections
+    cudaError_t e = launch_qk<T, D, G>(q, Hq, (alpha - 1.f) * scale, kv, ws, L,
+                                       cap * kv.P > kTpvSmemCand, s);
     if (e != cudaSuccess) return e;
     const int E = fabsf(alpha - 1.5f) < 1e-6f ? 2 : (fabsf(alpha - 2.f) < 1e-6f ? 1 : 0);
     if (E == 2) return launch_tpv<2, T, D>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
@@ -1528,7 +1590,7 @@ static cudaError_t launch_decode_softmax_t(const float* q, int Hq, float scale, 
                        cap, ws, L);
     }
     if (e != cudaSuccess) return e;
-    e = launch_qk<T, D, G>(q, Hq, scale, kv, ws, L, s);
+    e = launch_qk<T, D, G>(q, Hq, scale, kv, ws, L, false, s);
     if (e != cudaSuccess) return e;
     const int page_bytes = kv.P * D * (int)sizeof(T);
     const int ns = std::max(2, std::min(8, kPvStageBytes / page_bytes));   // 16 KiB fp32 pages: 2

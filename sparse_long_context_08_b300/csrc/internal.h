@@ -35,10 +35,14 @@ struct KV {
 //
 // The softmax decode adds partial-sum records (recs, nrec slots of G * (D + 1)
 // floats): one slot per streaming warp plus one per unit.
+//
+// pmax [U][Umax][G] holds each head's largest z' on each union page (-inf
+// where the head did not select it); plist [B * Hq][Umax] is the global page
+// list of the large-selection threshold kernel (with cand_x / cand_pos).
 struct DecodeLayout {
     int    U, G, Umax, nvw, ccap, nrec;
     size_t union_count, head_max, union_page, union_mask, union_blk, vtok, vrows;
-    size_t z, tau, cand_x, cand_pos, recs, total;
+    size_t z, pmax, tau, cand_x, cand_pos, plist, recs, total;
 };
 constexpr int kTpvSmemCand = 16384;      // candidates per head the shared-memory threshold kernel holds
 constexpr int kPvMaxWarps = 4096;        // streaming-warp record slots of the softmax decode

@@ -20,9 +20,11 @@ struct WS {
     uint32_t* vtok;       // [U][nvw] tokens whose V row was read
     int* vrows;           // per-unit popcount of vtok (measurement)
     float* z;             // [U][G][Umax * P]
+    float* pmax;          // [U][Umax][G] largest z' of each union page per head
     float* tau;
     float* cand_x;        // [B * Hq][ccap] candidates, then weights (large selections only)
     int* cand_pos;        // [B * Hq][ccap] their score index, then V row
+    int* plist;           // [B * Hq][Umax] pages that may hold candidates (large selections)
     float* recs;          // [nrec][G][D + 1] softmax partial sums (softmax decode only)
 };
 inline WS ws_views(void* base, const DecodeLayout& L) {
@@ -31,9 +33,10 @@ inline WS ws_views(void* base, const DecodeLayout& L) {
               reinterpret_cast<int*>(c + L.union_page), reinterpret_cast<int*>(c + L.union_mask),
               reinterpret_cast<int*>(c + L.union_blk), reinterpret_cast<uint32_t*>(c + L.vtok),
               reinterpret_cast<int*>(c + L.vrows), reinterpret_cast<float*>(c + L.z),
-              reinterpret_cast<float*>(c + L.tau),
+              reinterpret_cast<float*>(c + L.pmax), reinterpret_cast<float*>(c + L.tau),
               L.cand_x ? reinterpret_cast<float*>(c + L.cand_x) : nullptr,
               L.cand_pos ? reinterpret_cast<int*>(c + L.cand_pos) : nullptr,
+              L.plist ? reinterpret_cast<int*>(c + L.plist) : nullptr,
               L.recs ? reinterpret_cast<float*>(c + L.recs) : nullptr};
 }
 

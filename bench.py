@@ -168,21 +168,19 @@ def bus_id_of(dev: int) -> str | None:
         return None
 
 
-def measured_traffic(workload: str, kernel: str, batch: int):
-    """DRAM bytes (read + write) of one launch of `kernel` from the committed ncu
-    summary, scaled to the launch; None when there is no capture for this
-    workload, or the kernel's source has changed since it was taken."""
+def measured_traffic(kernel: str, units: int):
+    """DRAM bytes (read + write) of one launch of `kernel` that processes
+    `units` (union pages for qk / pv, metadata pages for score), from the
+    committed ncu summary's bytes per unit; None when there is no capture for
+    the kernel or its source has changed since it was taken."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            tr = json.load(f)
-        k = tr["kernels"][kernel]
-        if tr.get("workload") != workload or batch != tr.get("batch"):
-            return None
+            k = json.load(f)["kernels"][kernel]
         with open(os.path.join(ROOT, k["source"]), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest() != k["source_sha256"]:
                 return None
-        return int(k["bytes_per_launch"])
+        return int(round(float(k["bytes_per_unit"]) * units))
     except (OSError, KeyError, ValueError):
         return None
 
@@ -425,7 +423,8 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     dom_bytes = per_kernel_bytes.get(dom)
     achieved = dom_bytes / (mean[dom] * 1e-3) / 1e9 if dom_bytes else None
-    traffic = measured_traffic(args.workload, dom, w.batch)
+    traffic = measured_traffic(dom, {"qk": int(up.sum()), "score": pages}.get(dom, 0)) \
+        if dom in ("qk", "score") else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
                 "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,
@@ -613,7 +612,10 @@ def run_full(args):
     achieved = dom_bytes / (mean[dom] * 1e-3) / 1e9 if dom_bytes else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
-                "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                "peak_kind": f"{peak_kind} copy bandwidth",
+                "traffic": measured_traffic(dom, {"qk": int(up.sum()), "pv": int(up.sum()),
+                                                  "score": pages}.get(dom, 0))
+                if dom in ("qk", "pv", "score") else None,
                 "algorithmic_bytes": dom_bytes}
 
     e2e = None

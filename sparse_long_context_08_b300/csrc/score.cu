@@ -51,6 +51,15 @@ struct XRed {
     }
 };
 
+// d = a * b + d on both lanes of a float pair, one rounding each (paired fp32 FMA).
+__device__ __forceinline__ void fma2(float2& d, float2 a, float2 b) {
+    unsigned long long dd = *reinterpret_cast<unsigned long long*>(&d);
+    const unsigned long long aa = *reinterpret_cast<unsigned long long*>(&a);
+    const unsigned long long bb = *reinterpret_cast<unsigned long long*>(&b);
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(dd) : "l"(aa), "l"(bb));
+    d = *reinterpret_cast<float2*>(&dd);
+}
+
 template <typename T, int D, int G, bool kGauss>
 struct ScoreCfg {
     static constexpr int ES = sizeof(T);
@@ -200,17 +209,26 @@ score_kernel(const float* __restrict__ q, int Hq, float scale, KV kv,
                 float xa[C::DPL], xb[C::DPL];
                 widen_lane<T, C::DPL>(st, xa);
                 widen_lane<T, C::DPL>(st + 32 * CB, xb);
+                // paired FMAs over coordinate pairs: half the instructions,
+                // two independent chains per sum
 #pragma unroll
-                for (int h = 0; h < G; ++h)
+                for (int h = 0; h < G; ++h) {
+                    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < C::DPL; ++e) {
+                    for (int e = 0; e < C::DPL; e += 2) {
+                        const float2 ka = make_float2(xa[e], xa[e + 1]);
+                        const float2 kb = make_float2(xb[e], xb[e + 1]);
                         if constexpr (kGauss) {
-                            acc[h] = fmaf(qa[h][e], xa[e], acc[h]);
-                            acc[G + h] = fmaf(qb[h][e], xb[e], acc[G + h]);
+                            fma2(s0, make_float2(qa[h][e], qa[h][e + 1]), ka);
+                            fma2(s1, make_float2(qb[h][e], qb[h][e + 1]), kb);
                         } else {
-                            acc[h] = fmaf(qb[h][e], xa[e], fmaf(qa[h][e], xb[e], acc[h]));
+                            fma2(s0, make_float2(qa[h][e], qa[h][e + 1]), kb);
+                            fma2(s0, make_float2(qb[h][e], qb[h][e + 1]), ka);
                         }
                     }
+                    acc[h] = s0.x + s0.y;
+                    if constexpr (kGauss) acc[G + h] = s1.x + s1.y;
+                }
             }
             XRed<C::NV, C::LPR / 2>::run(acc, lt);
             if (inr && lt % DUP == 0) {

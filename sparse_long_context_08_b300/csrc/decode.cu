@@ -33,7 +33,7 @@ EKV_DEFINE_STATUS(decode)
 
 namespace ekv {
 
-constexpr int kPlanThreads = 256;
+constexpr int kPlanThreads = 512;
 constexpr int kQkConsumers = 12;                       // consumer warps per qk CTA
 constexpr int kQkThreads = 32 * (kQkConsumers + 1);    // + one producer warp
 constexpr int kQkGroup = 16;                           // pages resolved per producer step
@@ -41,8 +41,10 @@ constexpr int kQkMaxSlots = 48;
 constexpr int kQkSmemBudget = 220 * 1024;
 constexpr int kMaxUnits = 8192;                        // qk keeps a prefix over units in smem
 constexpr int kTpvThreads = 256;
+constexpr int kTpvgThreads = 512;                      // the global-candidate variant
 constexpr int kTpvVec = 8;                             // float4 per thread per score tile
 constexpr int kTpvTile = kTpvThreads * kTpvVec * 4;    // scores per tile
+constexpr int kTpvgTile = kTpvgThreads * kTpvVec * 4;
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -896,13 +898,13 @@ __global__ void count_rows_kernel(WS ws, DecodeLayout L) {
 constexpr int kTpvgRows = 4;          // V rows in flight per row group
 
 template <typename T, int D, int E>
-__global__ void __launch_bounds__(kTpvThreads)
+__global__ void __launch_bounds__(kTpvgThreads)
 tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __restrict__ out,
                   float* __restrict__ tau_out, int32_t* __restrict__ support_out) {
     pdl_enter();
     constexpr int EPC = Elem<T>::kPer16;
     constexpr int LPR = D / EPC;              // lanes per V row
-    constexpr int RG = kTpvThreads / LPR;     // row groups
+    constexpr int RG = kTpvgThreads / LPR;     // row groups
     __shared__ float s_red[RG * D];
     __shared__ float fred[40];
     __shared__ float2 f2red[32];
@@ -929,7 +931,7 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
     float pm[kTpvPmVec];
 #pragma unroll
     for (int j = 0; j < kTpvPmVec; ++j) {
-        const int i = j * kTpvThreads + tid;
+        const int i = j * kTpvgThreads + tid;
         pm[j] = i < L.Umax ? __ldcg(pmr + (int64_t)i * G) : -INFINITY;
     }
     const int n = ucnt * P;
@@ -950,12 +952,12 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
     const int npl = list_candidate_pages(pm, pmr, G, ucnt, mx, pl, ired);   // ends with a barrier
     int m = 0;
     const int ne = npl * P;
-    for (int t0 = 0; t0 < ne; t0 += kTpvTile) {
+    for (int t0 = 0; t0 < ne; t0 += kTpvgTile) {
         float v[kTpvVec * 4];
         int zi[kTpvVec];
 #pragma unroll
         for (int j = 0; j < kTpvVec; ++j) {
-            const int e = t0 + (j * kTpvThreads + tid) * 4;
+            const int e = t0 + (j * kTpvgThreads + tid) * 4;
             zi[j] = e < ne ? __ldcg(pl + e / P) * P + e % P : 0;
             const float4 f = e < ne ? __ldcg(reinterpret_cast<const float4*>(z + zi[j]))
                                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -1455,7 +1457,7 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
     if (cand_cap > kTpvSmemCand) {
         if (!ws.cand_x || !ws.plist || L.ccap < cand_cap) return cudaErrorInvalidValue;
         stage_mark(2, s);
-        e = launch_pdl(tpv_global_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvThreads), 0, s, Hq,
+        e = launch_pdl(tpv_global_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvgThreads), 0, s, Hq,
                        alpha, kv, ws, L, out, tau_out, support_out);
         if (e != cudaSuccess) return e;
         stage_mark(3, s);

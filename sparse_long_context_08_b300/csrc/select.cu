@@ -452,7 +452,7 @@ cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp,
                                int32_t* n_sel, float* aux, bool shared, cudaStream_t s) {
     // shared: one CTA per (sequence, kv head), G times fewer CTAs, so each
     // gets the most threads
-    const int threads = shared ? 1024 : (kv.maxp <= 8192 ? 256 : (kv.maxp <= 16384 ? 512 : 1024));
+    const int threads = shared ? 1024 : (kv.maxp <= 8192 ? 512 : 1024);
     const size_t smem = (size_t)kv.maxp * 4;
     if ((int)smem > max_optin_smem() - 4096) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,

@@ -453,7 +453,8 @@ def run_ours(args):
             dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
         e2e = {"value": float(t_e2e.item()) / K / world * 1e6, "unit": "us/step",
                "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4,
-               "timing": "host wall clock per step incl. H2D, the three calls, D2H and sync"}
+               "timing": "host wall clock per step: step_host (one graph replay of the pinned "
+                         "H2D of q, the step's kernels and the D2H of out) and the sync"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -639,7 +640,8 @@ def run_full(args):
             dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
         e2e = {"value": float(t_e2e.item()) / world * 1e6, "unit": "us/step",
                "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4,
-               "timing": "host wall clock per step incl. H2D, the calls, D2H and sync"}
+               "timing": "host wall clock per step: step_host (one graph replay of the pinned "
+                         "H2D of q, the kernels and the D2H of out) and the sync"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -11,6 +11,41 @@ import torch
 from . import entmaxkv as E
 
 
+class _HostStepGraphs:
+    """Replays a host-buffer step as one CUDA graph: the pinned H2D copy of q,
+    the step's kernels and the D2H copy of out are captured on the first call
+    with a given set of buffers, so later calls cost one graph launch instead
+    of one launch per copy and kernel.  The graph keeps the buffers it was
+    captured with: the same tensors must stay alive and be reused."""
+
+    def _host_graph_replay(self, eager, q_host, out_host, q_dev, stream=None) -> None:
+        last = self.__dict__.get("_host_last")
+        if (last is not None and stream is None and last[0] is q_host and last[1] is out_host
+                and last[2] is q_dev):
+            last[3].replay()                      # same buffers as the last call
+            return
+        graphs = self.__dict__.setdefault("_host_graphs", {})
+        key = (q_host.data_ptr(), out_host.data_ptr(), q_dev.data_ptr())
+        g = graphs.get(key)
+        if g is None:
+            cs = torch.cuda.Stream()
+            cs.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(cs):
+                eager(q_host, out_host, q_dev, cs)          # warm-up outside the capture
+            cs.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cs):
+                eager(q_host, out_host, q_dev, cs)
+            torch.cuda.current_stream().wait_stream(cs)
+            graphs[key] = g
+        self._host_last = (q_host, out_host, q_dev, g)
+        if stream is None:
+            g.replay()
+        else:
+            with torch.cuda.stream(stream):
+                g.replay()
+
+
 def upload_workload(w, device="cuda") -> tuple[E.PagedKV, torch.Tensor]:
     """Copy a workloads.Workload (host numpy arrays) to the GPU."""
     def pool(a):
@@ -25,7 +60,7 @@ def upload_workload(w, device="cuda") -> tuple[E.PagedKV, torch.Tensor]:
     return kv, q
 
 
-class EntmaxKVDecoder:
+class EntmaxKVDecoder(_HostStepGraphs):
     """score_pages -> select -> decode for one (cache, policy) configuration."""
 
     def __init__(self, kv: E.PagedKV, num_q_heads: int, scale: float, alpha: float,
@@ -82,18 +117,21 @@ class EntmaxKVDecoder:
         self.select(stream)
         return self.decode(q, stream)
 
-    def step_host(self, q_host: torch.Tensor, out_host: torch.Tensor, q_dev: torch.Tensor,
-                  stream=None) -> None:
-        """One decode step from host memory: q_host (pinned) -> device, the three
-        stages, then out -> out_host (pinned).  Asynchronous on `stream`."""
-        s = stream if stream is not None else torch.cuda.current_stream()
+    def _step_host_eager(self, q_host, out_host, q_dev, s) -> None:
         with torch.cuda.stream(s):
             q_dev.copy_(q_host, non_blocking=True)
             self.step(q_dev, s)
             out_host.copy_(self.out, non_blocking=True)
 
+    def step_host(self, q_host: torch.Tensor, out_host: torch.Tensor, q_dev: torch.Tensor,
+                  stream=None) -> None:
+        """One decode step from host memory: q_host (pinned) -> device, the three
+        stages, then out -> out_host (pinned).  Asynchronous on `stream`; replayed
+        as one CUDA graph per set of buffers (see _HostStepGraphs)."""
+        self._host_graph_replay(self._step_host_eager, q_host, out_host, q_dev, stream)
 
-class EntmaxKVFullDecoder:
+
+class EntmaxKVFullDecoder(_HostStepGraphs):
     """Full-cache alpha-entmax decode: attention over every valid token, the
     exact result the sparse pipeline approximates."""
 
@@ -118,18 +156,20 @@ class EntmaxKVFullDecoder:
                                self.support, self.workspace, stream)
         return self.out
 
-    def step_host(self, q_host: torch.Tensor, out_host: torch.Tensor, q_dev: torch.Tensor,
-                  stream=None) -> None:
-        """q_host (pinned) -> device, the full-cache decode, out -> out_host
-        (pinned).  Asynchronous on `stream`."""
-        s = stream if stream is not None else torch.cuda.current_stream()
+    def _step_host_eager(self, q_host, out_host, q_dev, s) -> None:
         with torch.cuda.stream(s):
             q_dev.copy_(q_host, non_blocking=True)
             self.decode(q_dev, s)
             out_host.copy_(self.out, non_blocking=True)
 
+    def step_host(self, q_host: torch.Tensor, out_host: torch.Tensor, q_dev: torch.Tensor,
+                  stream=None) -> None:
+        """q_host (pinned) -> device, the full-cache decode, out -> out_host
+        (pinned).  Asynchronous on `stream`; replayed as one CUDA graph."""
+        self._host_graph_replay(self._step_host_eager, q_host, out_host, q_dev, stream)
 
-class EntmaxKVSoftmaxDecoder:
+
+class EntmaxKVSoftmaxDecoder(_HostStepGraphs):
     """Softmax attention over the pages the EntmaxKV scoring and selection keep
     (the comparison method: a softmax whose dense tail is truncated to the kept
     pages), or over every token with full=True.  The selection stage is the
@@ -172,10 +212,14 @@ class EntmaxKVSoftmaxDecoder:
             self.sparse.select(stream)
         return self.decode(q, stream)
 
-    def step_host(self, q_host: torch.Tensor, out_host: torch.Tensor, q_dev: torch.Tensor,
-                  stream=None) -> None:
-        s = stream if stream is not None else torch.cuda.current_stream()
+    def _step_host_eager(self, q_host, out_host, q_dev, s) -> None:
         with torch.cuda.stream(s):
             q_dev.copy_(q_host, non_blocking=True)
             self.step(q_dev, s)
             out_host.copy_(self.out, non_blocking=True)
+
+    def step_host(self, q_host: torch.Tensor, out_host: torch.Tensor, q_dev: torch.Tensor,
+                  stream=None) -> None:
+        """q_host (pinned) -> device, the step, out -> out_host (pinned);
+        replayed as one CUDA graph."""
+        self._host_graph_replay(self._step_host_eager, q_host, out_host, q_dev, stream)

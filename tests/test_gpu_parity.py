@@ -413,6 +413,26 @@ def test_deterministic_across_runs():
         assert np.array_equal(a[k], b[k]), k
 
 
+def test_step_host_graph_matches_the_device_step():
+    """step_host replays its step (H2D of q, kernels, D2H of out) as one CUDA
+    graph; every call returns what the device step returns, bit for bit, and
+    follows new host inputs."""
+    w = make_workload("long128k", batch=2, context=8192)
+    g = GpuRun(w)
+    q_host = g.q.cpu().pin_memory()
+    out_host = torch.empty(g.dec.out.shape, dtype=torch.float32).pin_memory()
+    q_dev = torch.empty_like(g.q)
+    for it in range(3):
+        if it == 2:
+            q_host.copy_(q_host * 0.5)            # new input through the same buffers
+        g.dec.step_host(q_host, out_host, q_dev)
+        torch.cuda.synchronize()
+        got = out_host.clone()
+        g.dec.step(q_host.cuda())
+        torch.cuda.synchronize()
+        assert torch.equal(got, g.dec.out.cpu()), it
+
+
 def test_graph_capture_replays_the_step():
     w = make_workload("long128k", batch=2, context=8192)
     g = GpuRun(w)

@@ -78,6 +78,33 @@ def overrides(args) -> dict:
     return kw
 
 
+# ---------------------------------------------------------------------------
+# multi-rank helpers (replicas: every rank runs its own step, no data-path
+# collective; only the timing is combined)
+# ---------------------------------------------------------------------------
+def rank_seed(workload: str, rank: int) -> int:
+    """Each replica decodes its own synthetic cache."""
+    from sparse_long_context_08_b300.workloads import CONFIGS
+    return CONFIGS[workload]["seed"] + 1000 * rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (time of the timed region)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_us_per_step(ms_per_step_max: float, world: int) -> float:
+    """World ranks each ran the timed steps within the slowest rank's time:
+    microseconds per step of work over the whole job."""
+    return ms_per_step_max * 1e3 / world
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
             int(os.environ.get("WORLD_SIZE", 1)))
@@ -320,7 +347,7 @@ def run_ours(args):
     E.lib()
     from sparse_long_context_08_b300.workloads import CONFIGS
     kw = overrides(args)
-    w = make_workload(args.workload, seed=CONFIGS[args.workload]["seed"] + 1000 * rank, **kw)
+    w = make_workload(args.workload, seed=rank_seed(args.workload, rank), **kw)
     kv, q = upload_workload(w)
     dec = EntmaxKVDecoder(kv, w.num_q_heads, float(w.scale), w.alpha, w.policy,
                           w.budget_tokens, w.delta)
@@ -400,10 +427,7 @@ def run_ours(args):
         flush_l2(i + 3)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
-    t_sum = torch.tensor([sum(total)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t_sum, op=dist.ReduceOp.MAX)
-    ms_per_step = float(t_sum.item()) / K
+    ms_per_step = max_over_ranks(sum(total), world, "cuda") / K
 
     # bytes the step reads (metadata + selected pages + small tensors)
     up, vr = E.entmaxkv_decode_counts(dec.workspace, w.batch, w.num_q_heads, w.num_kv_heads,
@@ -448,10 +472,8 @@ def run_ours(args):
             dec.step_host(q_host, out_host, q_dev)
             stream.synchronize()
             times.append(time.perf_counter() - t0)
-        t_e2e = torch.tensor([sum(times)], dtype=torch.float64, device="cuda")
-        if world > 1:
-            dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
-        e2e = {"value": float(t_e2e.item()) / K / world * 1e6, "unit": "us/step",
+        e2e = {"value": whole_job_us_per_step(max_over_ranks(sum(times), world, "cuda") * 1e3 / K,
+                                              world), "unit": "us/step",
                "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4,
                "timing": "host wall clock per step: step_host (one graph replay of the pinned "
                          "H2D of q, the step's kernels and the D2H of out) and the sync"}
@@ -467,7 +489,7 @@ def run_ours(args):
         if world > 1:
             dist.destroy_process_group()
         return
-    value_us = ms_per_step * 1e3 / world
+    value_us = whole_job_us_per_step(ms_per_step, world)
     line = {
         "metric": METRIC, "value": value_us, "unit": "us/step", "n_gpus": world,
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
@@ -506,8 +528,7 @@ def run_full(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     E.lib()
-    w = make_workload(args.workload, seed=CONFIGS[args.workload]["seed"] + 1000 * rank,
-                      **overrides(args))
+    w = make_workload(args.workload, seed=rank_seed(args.workload, rank), **overrides(args))
     kv, q = upload_workload(w)
     mode = args.mode
     pre = []                                   # stages before the decode call
@@ -588,10 +609,7 @@ def run_full(args):
         flush_l2(i + 3)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
-    t_sum = torch.tensor([sum(total)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t_sum, op=dist.ReduceOp.MAX)
-    ms_per_step = float(t_sum.item()) / K
+    ms_per_step = max_over_ranks(sum(total), world, "cuda") / K
 
     up, vr = E.entmaxkv_decode_counts(dec.workspace, w.batch, w.num_q_heads, w.num_kv_heads,
                                       w.head_dim, w.page_size, w.max_pages, dec.cap if mode != "full"
@@ -635,10 +653,9 @@ def run_full(args):
             dec.step_host(q_host, out_host, q_dev)
             stream.synchronize()
             times.append(time.perf_counter() - t0)
-        t_e2e = torch.tensor([sum(times) / len(times)], dtype=torch.float64, device="cuda")
-        if world > 1:
-            dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
-        e2e = {"value": float(t_e2e.item()) / world * 1e6, "unit": "us/step",
+        e2e = {"value": whole_job_us_per_step(
+                   max_over_ranks(sum(times) / len(times), world, "cuda") * 1e3, world),
+               "unit": "us/step",
                "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4,
                "timing": "host wall clock per step: step_host (one graph replay of the pinned "
                          "H2D of q, the kernels and the D2H of out) and the sync"}
@@ -655,7 +672,8 @@ def run_full(args):
             dist.destroy_process_group()
         return
     line = {
-        "metric": MODE_METRIC[mode], "value": ms_per_step * 1e3 / world, "unit": "us/step",
+        "metric": MODE_METRIC[mode], "value": whole_job_us_per_step(ms_per_step, world),
+        "unit": "us/step",
         "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic", "config": dict(workload_config(w), mode=mode),

@@ -132,7 +132,7 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
                    int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
                    float* __restrict__ aux, int gs) {
     pdl_enter();
-    extern __shared__ __align__(16) uint32_t keys[];   // [max_pages]
+    extern __shared__ __align__(16) uint32_t keys[];   // [max_pages] keys, then [kp] selection
     __shared__ int hist[256];
     __shared__ uint32_t umin_red[32], umax_red[32];
     __shared__ int ired[40];
@@ -145,6 +145,7 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     const int np = min(kv.maxp, (kv.sl[b] + kv.P - 1) / kv.P);
     const float* src = bound + (int64_t)bh * kv.maxp;
     int32_t* dst = sel + (int64_t)bh * kp;
+    int32_t* s_sel = reinterpret_cast<int32_t*>(keys + kv.maxp);   // the row, written out coalesced
     const int k = min(kp, np);
     if (k <= 0) {
         if (tid < ng) {
@@ -272,10 +273,10 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
         const int rb = r + __popc(mb & below);     // boundary-bin keys before i
         bool take = false;
         if (in && kh > hi) {
-            dst[ra + min(rb, takeB)] = i;
+            s_sel[ra + min(rb, takeB)] = i;
             take = true;
         } else if (in && kh == hi && rb < takeB) {
-            dst[ra + rb] = i;
+            s_sel[ra + rb] = i;
             take = true;
         }
         if (take) tmin = min(tmin, key);
@@ -283,7 +284,8 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
         a += __popc(ma);
         r += __popc(mb);
     }
-    // smallest taken key (the k-th bound) and largest key left out
+    // smallest taken key (the k-th bound) and largest key left out; the
+    // barrier also completes s_sel
     const int any = __syncthreads_or(any_out);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -305,12 +307,10 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
             }
         }
     }
-    if (ng > 1) {                          // the other heads of the group get the same rows
-        __syncthreads();                   // this block's writes of row 0 are visible
-        for (int x = tid; x < (ng - 1) * k; x += nt) {
-            const int g = 1 + x / k, r = x - (g - 1) * k;
-            dst[(int64_t)g * kp + r] = dst[r];
-        }
+    // the row (and, shared, the group's other heads' copies) in whole sectors
+    for (int x = tid; x < ng * k; x += nt) {
+        const int g = x / k, r = x - g * k;
+        dst[(int64_t)g * kp + r] = s_sel[r];
     }
 }
 
@@ -453,7 +453,7 @@ cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp,
     // shared: one CTA per (sequence, kv head), G times fewer CTAs, so each
     // gets the most threads
     const int threads = shared ? 1024 : (kv.maxp <= 8192 ? 512 : 1024);
-    const size_t smem = (size_t)kv.maxp * 4;
+    const size_t smem = (size_t)kv.maxp * 4 + (size_t)kp * 4;
     if ((int)smem > max_optin_smem() - 4096) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -324,6 +324,15 @@ __device__ __forceinline__ uint32_t split_term(float x, int s) {
     return s == 0 ? hi : (s == 1 ? mid : lo);
 }
 
+// d = a * b + d on both lanes of a float pair, one rounding each (paired fp32 FMA).
+__device__ __forceinline__ void fma2(float2& d, float2 a, float2 b) {
+    unsigned long long dd = *reinterpret_cast<unsigned long long*>(&d);
+    const unsigned long long aa = *reinterpret_cast<unsigned long long*>(&a);
+    const unsigned long long bb = *reinterpret_cast<unsigned long long*>(&b);
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(dd) : "l"(aa), "l"(bb));
+    d = *reinterpret_cast<float2*>(&dd);
+}
+
 // c += A (16 x 16, row) * B (16 x 8, col), bf16 operands, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(

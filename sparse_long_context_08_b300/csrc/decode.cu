@@ -1198,7 +1198,7 @@ pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
         return dsc;
     };
 
-    float acc[G][DPL];
+    float2 acc[G][DPL / 2];       // coordinate pairs (paired FMAs)
     float lsum[NW];               // this lane's share of sum_t w for head (lane + 32 j) / 32 ... see below
     float mh[G];
     int cur_u = -1, slot = -1;
@@ -1207,7 +1207,10 @@ pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) rec[g * D + lane * DPL + e] = acc[g][e];
+            for (int e = 0; e < DPL / 2; ++e) {
+                rec[g * D + lane * DPL + 2 * e] = acc[g][e].x;
+                rec[g * D + lane * DPL + 2 * e + 1] = acc[g][e].y;
+            }
         // weight index x = lane + 32 j covers head x / 32 (token x % 32)
 #pragma unroll
         for (int j = 0; j < NW; ++j) {
@@ -1215,10 +1218,21 @@ pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
             if (lane == 0 && j < G) rec[G * D + j] = l;
         }
     };
+    // scores of a page for this lane's weights: entry j = head j, token lane
+    // (-inf where the head did not select the page or the token is past the end)
+    auto load_z = [&](const PgDesc& dd, float (&zz)[NW]) {
+        const float* zrow = ws.z + ((int64_t)dd.u * G) * L.Umax * P + (int64_t)dd.i * P;
+#pragma unroll
+        for (int j = 0; j < NW; ++j)
+            zz[j] = (dd.blk >= 0 && j < G && lane < P && lane < dd.valid && ((dd.mask >> j) & 1))
+                        ? __ldcg(zrow + (int64_t)j * L.Umax * P + lane) : -INFINITY;
+    };
     PgDesc dq[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x)
         if (x < ns - 1) dq[x] = issue(x);
+    float zc[NW];                 // the current page's scores, loaded one page ahead
+    load_z(dq[0], zc);
     bool failed = false;
     for (int k = 0; k < npg; ++k) {
         const int st = k % ns;
@@ -1229,10 +1243,15 @@ pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
             for (int x = 0; x < 8; ++x)
                 if (x == nst) dq[x] = nd;
         }
-        PgDesc d{};
+        PgDesc d{}, dn{};
+        const int nxs = (k + 1) % ns;
 #pragma unroll
-        for (int x = 0; x < 8; ++x)
+        for (int x = 0; x < 8; ++x) {
             if (x == st) d = dq[x];
+            if (x == nxs) dn = dq[x];
+        }
+        float zn[NW];
+        if (k + 1 < npg) load_z(dn, zn);
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[st], (uint32_t)((k / ns) & 1)))) {
             failed = true;
             break;
@@ -1247,27 +1266,23 @@ pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
                 const uint32_t key = __ldcg(ws.head_max + b * Hq + kvh * G + g);
                 mh[g] = key == 0u ? 0.f : key_float(key);      // no score: every weight is 0
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[g][e] = 0.f;
+                for (int e = 0; e < DPL / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
             }
 #pragma unroll
             for (int j = 0; j < NW; ++j) lsum[j] = 0.f;
         }
-        // weights of the page: entry x = lane + 32 j is head x / 32, token x % 32
-        const float* zrow = ws.z + ((int64_t)d.u * G) * L.Umax * P + (int64_t)d.i * P;
+        // weights of the page: entry j is head j, token lane
 #pragma unroll
         for (int j = 0; j < NW; ++j) {
-            const int g = j, t = lane;
-            float w = 0.f;
-            if (g < G && t < P && t < d.valid && ((d.mask >> g) & 1)) {
-                const float z = __ldcg(zrow + (int64_t)g * L.Umax * P + t);
-                w = __expf(z - mh[g]);
-            }
-            if (g < G && t < P) s_w[warp][t * G + g] = w;
+            const float w = (j < G && lane < P) ? __expf(zc[j] - mh[j]) : 0.f;   // e^-inf = 0
+            if (j < G && lane < P) s_w[warp][lane * G + j] = w;
             lsum[j] += w;
+            zc[j] = zn[j];
         }
         __syncwarp();
         const unsigned char* pg = ring + (size_t)st * page_bytes + (size_t)lane * DPL * sizeof(T);
         const int nt = d.blk >= 0 ? d.valid : 0;
+#pragma unroll 4
         for (int t = 0; t < nt; ++t) {
             float v[DPL];
             load_dpl<T, DPL>(pg + (size_t)t * D * sizeof(T), v);
@@ -1276,7 +1291,8 @@ pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
             for (int g = 0; g < G; ++g) {
                 const float w = wt[g];
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[g][e] = fmaf(w, v[e], acc[g][e]);
+                for (int e = 0; e < DPL / 2; ++e)
+                    fma2(acc[g][e], make_float2(w, w), make_float2(v[2 * e], v[2 * e + 1]));
             }
         }
         __syncwarp();        // every lane is done with stage st and s_w before they are refilled

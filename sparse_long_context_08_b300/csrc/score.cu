@@ -51,15 +51,6 @@ struct XRed {
     }
 };
 
-// d = a * b + d on both lanes of a float pair, one rounding each (paired fp32 FMA).
-__device__ __forceinline__ void fma2(float2& d, float2 a, float2 b) {
-    unsigned long long dd = *reinterpret_cast<unsigned long long*>(&d);
-    const unsigned long long aa = *reinterpret_cast<unsigned long long*>(&a);
-    const unsigned long long bb = *reinterpret_cast<unsigned long long*>(&b);
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(dd) : "l"(aa), "l"(bb));
-    d = *reinterpret_cast<float2*>(&dd);
-}
-
 template <typename T, int D, int G, bool kGauss>
 struct ScoreCfg {
     static constexpr int ES = sizeof(T);

@@ -45,6 +45,7 @@ constexpr int kTpvgThreads = 512;                      // the global-candidate v
 constexpr int kTpvVec = 8;                             // float4 per thread per score tile
 constexpr int kTpvTile = kTpvThreads * kTpvVec * 4;    // scores per tile
 constexpr int kTpvgTile = kTpvgThreads * kTpvVec * 4;
+constexpr int kTpvgRows = 4;                           // V rows in flight per row group (tpv kernels)
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -848,15 +849,27 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
     float acc[EPC];
 #pragma unroll
     for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
-    for (int i = rg; i < m; i += RG) {
-        const float w = s_x[i];
-        const int row = s_pos[i];
-        if (w > 0.f && row >= 0) {
-            float x[EPC];
-            Elem<T>::widen(ld_nc_v4(vbase + (int64_t)row * D + lr * EPC), x);
+    for (int i0 = rg; i0 < m; i0 += RG * kTpvgRows) {        // kTpvgRows V rows in flight
+        float w[kTpvgRows];
+        int row[kTpvgRows];
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+        for (int k = 0; k < kTpvgRows; ++k) {
+            const int i = i0 + k * RG;
+            w[k] = i < m ? s_x[i] : 0.f;
+            row[k] = i < m ? s_pos[i] : -1;
         }
+        uint4 r[kTpvgRows];
+#pragma unroll
+        for (int k = 0; k < kTpvgRows; ++k)
+            if (w[k] > 0.f && row[k] >= 0) r[k] = ld_nc_v4(vbase + (int64_t)row[k] * D + lr * EPC);
+#pragma unroll
+        for (int k = 0; k < kTpvgRows; ++k)
+            if (w[k] > 0.f && row[k] >= 0) {
+                float x[EPC];
+                Elem<T>::widen(r[k], x);
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc[e] = fmaf(w[k], x[e], acc[e]);
+            }
     }
 #pragma unroll
     for (int e = 0; e < EPC; ++e) s_red[rg * D + lr * EPC + e] = acc[e];
@@ -895,7 +908,6 @@ __global__ void count_rows_kernel(WS ws, DecodeLayout L) {
 // memory does.  Candidates, then weights, live in the head's ccap-entry slice
 // of cand_x / cand_pos; every threshold iteration re-reads them (L2).
 // ---------------------------------------------------------------------------
-constexpr int kTpvgRows = 4;          // V rows in flight per row group
 
 template <typename T, int D, int E>
 __global__ void __launch_bounds__(kTpvgThreads)

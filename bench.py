@@ -364,10 +364,9 @@ def run_ours(args):
         flush_read.sum(dtype=torch.int32)
     stream = torch.cuda.current_stream()
 
-    # Two CUDA graphs of the step: the plain one (kernels chained by
-    # programmatic dependent launch) is the one timed for the headline; a copy
-    # with event-record nodes at the stage boundaries times score | select |
-    # plan | qk | tpv (those nodes serialise the kernels, so its total is a
+    # Two CUDA graphs of the step: the plain one (the five kernels back to back)
+    # is the one timed for the headline; a copy with event-record nodes at the
+    # stage boundaries times score | select | plan | qk | tpv (its total is a
     # little longer).
     evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
     for x in evs:

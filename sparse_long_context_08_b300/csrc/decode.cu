@@ -97,7 +97,6 @@ template <int G>
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(KV kv, int Hq, const int32_t* __restrict__ sel, const int32_t* __restrict__ n_sel,
             int cap, WS ws, DecodeLayout L) {
-    pdl_enter();
     extern __shared__ __align__(16) uint32_t s_plan[];   // bitmaps, then union pages
     __shared__ int red[40];
     __shared__ int s_ns[G];
@@ -114,7 +113,6 @@ constexpr int kPlanAllChunk = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads)
 plan_all_kernel(KV kv, int Hq, WS ws, DecodeLayout L) {
-    pdl_enter();
     const int u = blockIdx.x, c = blockIdx.y, nc = gridDim.y;
     const int b = u / kv.hkv, kvh = u - b * kv.hkv;
     const int G = L.G;
@@ -189,7 +187,6 @@ template <typename T, int D, int G>
 __global__ void __launch_bounds__(kQkThreads, 1)
 qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, DecodeLayout L,
           int nslots, int group, int write_pm) {
-    pdl_enter();
     using C = QkCfg<T, D, G>;
     extern __shared__ __align__(128) unsigned char s_raw[];
     __shared__ int red[40];
@@ -434,7 +431,6 @@ template <int D, int G, bool kPM>      // kPM: also write each head's page maxim
 __global__ void __launch_bounds__(kQmWarps * 32, kQmCtasPerSm)
 qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, DecodeLayout L,
               int ns) {
-    pdl_enter();
     using C = QmCfg<D, G>;
     extern __shared__ __align__(128) unsigned char s_qm[];
     __shared__ int red[40];
@@ -669,7 +665,6 @@ template <typename T, int D, int E>   // E: 2 alpha = 1.5, 1 alpha = 2, 0 any ot
 __global__ void __launch_bounds__(kTpvThreads)
 tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
            float* __restrict__ out, float* __restrict__ tau_out, int32_t* __restrict__ support_out) {
-    pdl_enter();
     constexpr int EPC = Elem<T>::kPer16;
     constexpr int LPR = D / EPC;              // lanes per V row
     constexpr int RG = kTpvThreads / LPR;     // V rows per pass
@@ -913,7 +908,6 @@ template <typename T, int D, int E>
 __global__ void __launch_bounds__(kTpvgThreads)
 tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __restrict__ out,
                   float* __restrict__ tau_out, int32_t* __restrict__ support_out) {
-    pdl_enter();
     constexpr int EPC = Elem<T>::kPer16;
     constexpr int LPR = D / EPC;              // lanes per V row
     constexpr int RG = kTpvgThreads / LPR;     // row groups
@@ -1141,7 +1135,6 @@ __device__ __forceinline__ void load_dpl(const unsigned char* p, float (&x)[DPL]
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kPvWarps * 32, kPvCtasPerSm)
 pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
-    pdl_enter();
     constexpr int DPL = D / 32;
     constexpr int NW = (32 * G + 31) / 32;        // weights per lane per page (P <= 32)
     extern __shared__ __align__(128) unsigned char s_pv[];
@@ -1320,7 +1313,6 @@ pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
 __global__ void __launch_bounds__(128)
 softmax_merge_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int nwg, float* __restrict__ out,
                      float* __restrict__ lse_out) {
-    pdl_enter();
     __shared__ int red[40];
     __shared__ int s_w[1024];
     __shared__ int s_n;
@@ -1485,7 +1477,7 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
     if (cand_cap > kTpvSmemCand) {
         if (!ws.cand_x || !ws.plist || L.ccap < cand_cap) return cudaErrorInvalidValue;
         stage_mark(2, s);
-        e = launch_pdl(tpv_global_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvgThreads), 0, s, Hq,
+        e = launch_kernel(tpv_global_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvgThreads), 0, s, Hq,
                        alpha, kv, ws, L, out, tau_out, support_out);
         if (e != cudaSuccess) return e;
         stage_mark(3, s);
@@ -1496,7 +1488,7 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     stage_mark(2, s);
-    e = launch_pdl(tpv_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvThreads), smem, s, Hq, alpha,
+    e = launch_kernel(tpv_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvThreads), smem, s, Hq, alpha,
                    cand_cap, kv, ws, L, out, tau_out, support_out);
     if (e != cudaSuccess) return e;
     stage_mark(3, s);
@@ -1518,7 +1510,7 @@ static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv,
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
-        e = launch_pdl(kernel, dim3(sm_count() * kQmCtasPerSm), dim3(kQmWarps * 32), smem, s, q, Hq,
+        e = launch_kernel(kernel, dim3(sm_count() * kQmCtasPerSm), dim3(kQmWarps * 32), smem, s, q, Hq,
                        qscale, kv, ws, L, ns);
         if (e != cudaSuccess) return e;
     } else {
@@ -1532,7 +1524,7 @@ static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv,
         e = cudaFuncSetAttribute(qk_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
-        e = launch_pdl(qk_kernel<T, D, G>, dim3(sm_count()), dim3(kQkThreads), smem, s, q, Hq,
+        e = launch_kernel(qk_kernel<T, D, G>, dim3(sm_count()), dim3(kQkThreads), smem, s, q, Hq,
                        qscale, kv, ws, L, ns, std::min(kQkGroup, ns), pm ? 1 : 0);
         if (e != cudaSuccess) return e;
     }
@@ -1565,7 +1557,7 @@ static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV
     const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax);
     e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel, cap,
+    e = launch_kernel(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel, cap,
                    ws, L);
     if (e != cudaSuccess) return e;
     return launch_qk_tpv<T, D, G>(q, Hq, scale, kv, cap, alpha, out, tau_out, support_out, ws, L, s);
@@ -1579,7 +1571,7 @@ static cudaError_t launch_decode_full_t(const float* q, int Hq, float scale, con
     if (L.U > kMaxUnits || L.Umax != kv.maxp) return cudaErrorInvalidValue;
     stage_mark(0, s);
     const int chunks = (kv.maxp + kPlanAllChunk - 1) / kPlanAllChunk;
-    cudaError_t e = launch_pdl(plan_all_kernel, dim3(L.U, chunks), dim3(kPlanThreads), 0, s, kv, Hq,
+    cudaError_t e = launch_kernel(plan_all_kernel, dim3(L.U, chunks), dim3(kPlanThreads), 0, s, kv, Hq,
                                ws, L);
     if (e != cudaSuccess) return e;
     return launch_qk_tpv<T, D, G>(q, Hq, scale, kv, kv.maxp, alpha, out, tau_out, support_out, ws,
@@ -1610,13 +1602,13 @@ static cudaError_t launch_decode_softmax_t(const float* q, int Hq, float scale, 
     if (full) {
         if (L.Umax != kv.maxp) return cudaErrorInvalidValue;
         const int chunks = (kv.maxp + kPlanAllChunk - 1) / kPlanAllChunk;
-        e = launch_pdl(plan_all_kernel, dim3(L.U, chunks), dim3(kPlanThreads), 0, s, kv, Hq, ws, L);
+        e = launch_kernel(plan_all_kernel, dim3(L.U, chunks), dim3(kPlanThreads), 0, s, kv, Hq, ws, L);
     } else {
         if (cap > kPlanSelRegs * kPlanThreads / G) return cudaErrorInvalidValue;
         const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax);
         e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        e = launch_pdl(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel,
+        e = launch_kernel(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel,
                        cap, ws, L);
     }
     if (e != cudaSuccess) return e;
@@ -1630,10 +1622,10 @@ static cudaError_t launch_decode_softmax_t(const float* q, int Hq, float scale, 
                              (int)smem);
     if (e != cudaSuccess) return e;
     stage_mark(2, s);
-    e = launch_pdl(pv_softmax_kernel<T, D, G>, dim3(grid), dim3(kPvWarps * 32), smem, s, Hq, kv, ws,
+    e = launch_kernel(pv_softmax_kernel<T, D, G>, dim3(grid), dim3(kPvWarps * 32), smem, s, Hq, kv, ws,
                    L, ns);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(softmax_merge_kernel, dim3(kv.B * Hq), dim3(128), 0, s, Hq, kv, ws, L,
+    e = launch_kernel(softmax_merge_kernel, dim3(kv.B * Hq), dim3(128), 0, s, Hq, kv, ws, L,
                    grid * kPvWarps, out, lse_out);
     if (e != cudaSuccess) return e;
     stage_mark(3, s);

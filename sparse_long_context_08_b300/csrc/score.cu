@@ -95,7 +95,6 @@ score_kernel(const float* __restrict__ q, int Hq, float scale, KV kv,
              const T* __restrict__ ma,      // bbox: kmin   gauss: mean
              const T* __restrict__ mb,      // bbox: kmax   gauss: var
              float* __restrict__ out, int nloc_max) {
-    pdl_enter();
     using C = ScoreCfg<T, D, G, kGauss>;
     constexpr int S = kScoreStages;
     constexpr int CB = C::DPL * sizeof(T);      // bytes a lane copies per row
@@ -264,7 +263,7 @@ static cudaError_t launch_score_t(const float* q, int Hq, float scale, const KV&
     cudaError_t e = cudaFuncSetAttribute(score_kernel<T, D, G, kGauss>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(score_kernel<T, D, G, kGauss>, dim3(grid), dim3(kScoreThreads), smem, s, q, Hq,
+    return launch_kernel(score_kernel<T, D, G, kGauss>, dim3(grid), dim3(kScoreThreads), smem, s, q, Hq,
                       scale, kv, static_cast<const T*>(ma), static_cast<const T*>(mb), out,
                       nloc_max);
 }

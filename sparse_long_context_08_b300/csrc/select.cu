@@ -131,7 +131,6 @@ __global__ void __launch_bounds__(kTopkMaxThreads)
 select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
                    int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
                    float* __restrict__ aux, int gs) {
-    pdl_enter();
     extern __shared__ __align__(16) uint32_t keys[];   // [max_pages] keys, then [kp] selection
     __shared__ int hist[256];
     __shared__ uint32_t umin_red[32], umax_red[32];
@@ -338,7 +337,6 @@ __global__ void __launch_bounds__(kSelThreads)
 select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float alpha,
                     float delta, int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
                     float* __restrict__ aux) {
-    pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ SelShared sh;
     __shared__ float2 fred[32];
@@ -459,7 +457,7 @@ cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int gs = shared ? Hq / kv.hkv : 0;
-    return launch_pdl(select_topk_kernel, dim3(shared ? kv.B * kv.hkv : kv.B * Hq), dim3(threads),
+    return launch_kernel(select_topk_kernel, dim3(shared ? kv.B * kv.hkv : kv.B * Hq), dim3(threads),
                       smem, s, bound, kv, Hq, kp, sel, n_sel, aux, gs);
 }
 
@@ -475,14 +473,14 @@ cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, 
         e = cudaFuncSetAttribute(select_gauss_kernel<2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        e = launch_pdl(select_gauss_kernel<2>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
+        e = launch_kernel(select_gauss_kernel<2>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
                        Hq, cap, alpha, delta, sel, n_sel, aux);
         if (e != cudaSuccess) return e;
     } else {
         e = cudaFuncSetAttribute(select_gauss_kernel<1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        e = launch_pdl(select_gauss_kernel<1>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
+        e = launch_kernel(select_gauss_kernel<1>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
                        Hq, cap, alpha, delta, sel, n_sel, aux);
         if (e != cudaSuccess) return e;
     }

@@ -1478,7 +1478,7 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
         if (!ws.cand_x || !ws.plist || L.ccap < cand_cap) return cudaErrorInvalidValue;
         stage_mark(2, s);
         e = launch_kernel(tpv_global_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvgThreads), 0, s, Hq,
-                       alpha, kv, ws, L, out, tau_out, support_out);
+                          alpha, kv, ws, L, out, tau_out, support_out);
         if (e != cudaSuccess) return e;
         stage_mark(3, s);
         return cudaSuccess;
@@ -1489,7 +1489,7 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
     if (e != cudaSuccess) return e;
     stage_mark(2, s);
     e = launch_kernel(tpv_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvThreads), smem, s, Hq, alpha,
-                   cand_cap, kv, ws, L, out, tau_out, support_out);
+                      cand_cap, kv, ws, L, out, tau_out, support_out);
     if (e != cudaSuccess) return e;
     stage_mark(3, s);
     return cudaSuccess;
@@ -1511,7 +1511,7 @@ static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv,
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
         e = launch_kernel(kernel, dim3(sm_count() * kQmCtasPerSm), dim3(kQmWarps * 32), smem, s, q, Hq,
-                       qscale, kv, ws, L, ns);
+                          qscale, kv, ws, L, ns);
         if (e != cudaSuccess) return e;
     } else {
         const size_t page_bytes = (size_t)kv.P * D * sizeof(T);
@@ -1525,7 +1525,7 @@ static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv,
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
         e = launch_kernel(qk_kernel<T, D, G>, dim3(sm_count()), dim3(kQkThreads), smem, s, q, Hq,
-                       qscale, kv, ws, L, ns, std::min(kQkGroup, ns), pm ? 1 : 0);
+                          qscale, kv, ws, L, ns, std::min(kQkGroup, ns), pm ? 1 : 0);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -1558,7 +1558,7 @@ static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV
     e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = launch_kernel(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel, cap,
-                   ws, L);
+                      ws, L);
     if (e != cudaSuccess) return e;
     return launch_qk_tpv<T, D, G>(q, Hq, scale, kv, cap, alpha, out, tau_out, support_out, ws, L, s);
 }
@@ -1572,7 +1572,7 @@ static cudaError_t launch_decode_full_t(const float* q, int Hq, float scale, con
     stage_mark(0, s);
     const int chunks = (kv.maxp + kPlanAllChunk - 1) / kPlanAllChunk;
     cudaError_t e = launch_kernel(plan_all_kernel, dim3(L.U, chunks), dim3(kPlanThreads), 0, s, kv, Hq,
-                               ws, L);
+                                  ws, L);
     if (e != cudaSuccess) return e;
     return launch_qk_tpv<T, D, G>(q, Hq, scale, kv, kv.maxp, alpha, out, tau_out, support_out, ws,
                                   L, s);
@@ -1609,7 +1609,7 @@ static cudaError_t launch_decode_softmax_t(const float* q, int Hq, float scale, 
         e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         e = launch_kernel(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel,
-                       cap, ws, L);
+                          cap, ws, L);
     }
     if (e != cudaSuccess) return e;
     e = launch_qk<T, D, G>(q, Hq, scale, kv, ws, L, false, s);
@@ -1623,10 +1623,10 @@ static cudaError_t launch_decode_softmax_t(const float* q, int Hq, float scale, 
     if (e != cudaSuccess) return e;
     stage_mark(2, s);
     e = launch_kernel(pv_softmax_kernel<T, D, G>, dim3(grid), dim3(kPvWarps * 32), smem, s, Hq, kv, ws,
-                   L, ns);
+                      L, ns);
     if (e != cudaSuccess) return e;
     e = launch_kernel(softmax_merge_kernel, dim3(kv.B * Hq), dim3(128), 0, s, Hq, kv, ws, L,
-                   grid * kPvWarps, out, lse_out);
+                      grid * kPvWarps, out, lse_out);
     if (e != cudaSuccess) return e;
     stage_mark(3, s);
     return cudaSuccess;

@@ -264,8 +264,8 @@ static cudaError_t launch_score_t(const float* q, int Hq, float scale, const KV&
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(score_kernel<T, D, G, kGauss>, dim3(grid), dim3(kScoreThreads), smem, s, q, Hq,
-                      scale, kv, static_cast<const T*>(ma), static_cast<const T*>(mb), out,
-                      nloc_max);
+                         scale, kv, static_cast<const T*>(ma), static_cast<const T*>(mb), out,
+                         nloc_max);
 }
 
 cudaError_t launch_score(const float* q, int Hq, float scale, const KV& kv, const void* kmin,

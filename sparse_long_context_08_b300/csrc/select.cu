@@ -134,7 +134,6 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     extern __shared__ __align__(16) uint32_t keys[];   // [max_pages] keys, then [kp] selection
     __shared__ int hist[256];
     __shared__ uint32_t umin_red[32], umax_red[32];
-    __shared__ int ired[40];
     __shared__ int s_digit, s_above;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nt = blockDim.x, nwarps = nt >> 5;
@@ -458,7 +457,7 @@ cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp,
     if (e != cudaSuccess) return e;
     const int gs = shared ? Hq / kv.hkv : 0;
     return launch_kernel(select_topk_kernel, dim3(shared ? kv.B * kv.hkv : kv.B * Hq), dim3(threads),
-                      smem, s, bound, kv, Hq, kp, sel, n_sel, aux, gs);
+                         smem, s, bound, kv, Hq, kp, sel, n_sel, aux, gs);
 }
 
 cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, float alpha,
@@ -474,14 +473,14 @@ cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, 
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         e = launch_kernel(select_gauss_kernel<2>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
-                       Hq, cap, alpha, delta, sel, n_sel, aux);
+                          Hq, cap, alpha, delta, sel, n_sel, aux);
         if (e != cudaSuccess) return e;
     } else {
         e = cudaFuncSetAttribute(select_gauss_kernel<1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         e = launch_kernel(select_gauss_kernel<1>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
-                       Hq, cap, alpha, delta, sel, n_sel, aux);
+                          Hq, cap, alpha, delta, sel, n_sel, aux);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

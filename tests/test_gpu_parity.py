@@ -346,6 +346,28 @@ def test_budget_covers_every_page_and_single_page_sequences():
         assert r["aux"][bh, 1] == -np.inf
 
 
+def test_zero_length_sequence_in_a_batch():
+    """A sequence with no tokens: no pages scored or selected, out = 0, tau =
+    +inf, support 0, on every path; the other sequences match the oracle."""
+    w = make_workload("long128k", batch=3, seq_lens=[5000, 0, 3000], planted_pages=2)
+    rep = full_parity(w, heads=[h for h in range(3 * w.num_q_heads) if h // w.num_q_heads != 1])
+    g = GpuRun(w)
+    r = g.step()
+    Hq = w.num_q_heads
+    assert np.all(r["n_sel"][Hq:2 * Hq] == 0)
+    assert np.all(r["out"][Hq:2 * Hq] == 0) and np.all(np.isinf(r["tau"][Hq:2 * Hq]))
+    assert np.all(r["support"][Hq:2 * Hq] == 0)
+    from sparse_long_context_08_b300.api import EntmaxKVFullDecoder, EntmaxKVSoftmaxDecoder
+    full = EntmaxKVFullDecoder(g.kv, Hq, float(w.scale), w.alpha)
+    full.decode(g.q)
+    sm = EntmaxKVSoftmaxDecoder(g.kv, Hq, float(w.scale), w.policy, w.budget_tokens, full=True)
+    sm.decode(g.q)
+    torch.cuda.synchronize()
+    assert torch.all(full.out[1] == 0) and torch.all(torch.isinf(full.tau[1]))
+    assert torch.all(sm.out[1] == 0) and torch.all(torch.isinf(sm.lse[1]))
+    assert E.entmaxkv_read_device_status() == E.EKV_OK
+
+
 def test_empty_selection_gives_zero_output():
     w = make_workload("long128k", batch=1, context=2048)
     g = GpuRun(w)

@@ -18,7 +18,7 @@ EKV_DEFINE_STATUS(select)
 
 namespace ekv {
 
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 512;   // Gaussian select: two CTAs per SM (63 registers)
 
 struct SelShared {
     int red[40];
@@ -316,29 +316,46 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
 //   e = 2: E = (a^2 + sig^2) Phi(u) + a sig phi(u),   -dE = 2 (a Phi(u) + sig phi(u))
 //   e = 1: E = a Phi(u) + sig phi(u),                  -dE = Phi(u)
 // with a = mu - tau, u = a / sig; sig = 0 gives (a)_+^e.
+// Also returns the second derivative d2E/dtau^2 (z): e = 2: 2 Phi(u);
+// e = 1: phi(u) / sig (sig = 0: 2 [a > 0] and 0, the kinks aside).
 template <int E>
-__device__ __forceinline__ float2 gauss_moment(float mu, float sig, float tau) {
+__device__ __forceinline__ float3 gauss_moment(float mu, float sig, float tau) {
     const float a = mu - tau;
     if (!(sig > 0.f)) {
         const float ap = fmaxf(a, 0.f);
-        return E == 2 ? make_float2(ap * ap, 2.f * ap) : make_float2(ap, a > 0.f ? 1.f : 0.f);
+        return E == 2 ? make_float3(ap * ap, 2.f * ap, a > 0.f ? 2.f : 0.f)
+                      : make_float3(ap, a > 0.f ? 1.f : 0.f, 0.f);
     }
     const float u = a / sig;
     const float Phi = 0.5f * erfcf(-u * 0.70710678118654752f);
     const float phi = 0.39894228040143268f * expf(-0.5f * u * u);
     const float m1 = fmaf(a, Phi, sig * phi);
-    if (E == 2) return make_float2(fmaf(fmaf(a, a, sig * sig), Phi, a * sig * phi), 2.f * m1);
-    return make_float2(m1, Phi);
+    if (E == 2)
+        return make_float3(fmaf(fmaf(a, a, sig * sig), Phi, a * sig * phi), 2.f * m1, 2.f * Phi);
+    return make_float3(m1, Phi, phi / sig);
+}
+
+// Block-wide sum of a float3; `red` >= 32 float4.  Every thread calls it.
+__device__ __forceinline__ float3 block_sum3(float3 v, float4* red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v.x = warp_sum(v.x);
+    v.y = warp_sum(v.y);
+    v.z = warp_sum(v.z);
+    __syncthreads();
+    if (lane == 0) red[wid] = make_float4(v.x, v.y, v.z, 0.f);
+    __syncthreads();
+    const float4 r = lane < nw ? red[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    return make_float3(warp_sum(r.x), warp_sum(r.y), warp_sum(r.z));
 }
 
 template <int E>
-__global__ void __launch_bounds__(kSelThreads)
+__global__ void __launch_bounds__(kSelThreads, 2)
 select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float alpha,
                     float delta, int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
                     float* __restrict__ aux) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ SelShared sh;
-    __shared__ float2 fred[32];
+    __shared__ float4 fred[32];
     __shared__ float fmaxred[32];
     const int nw = blockDim.x >> 5;
     int* whist = reinterpret_cast<int*>(smem_raw);
@@ -375,22 +392,37 @@ select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float 
         return;
     }
 
-    // safeguarded Newton on the convex, decreasing F
-    float lo = mu_max - 1.f, hi = INFINITY, tau = lo;
+    // safeguarded Halley iteration on the convex, decreasing F (F, its slope
+    // -dF and curvature H come from the same pass over the pages).  mu_max - 1
+    // is a lower bound of the root: the page holding mu_max alone gives
+    // E[(X - mu_max + 1)_+^e] >= 1 by Jensen.  Starting at mu_max, where
+    // the roots of these score distributions sit within a fraction of 1,
+    // saves the climb from the bound.
+    float lo = mu_max - 1.f, hi = INFINITY, tau = mu_max;
     for (int it = 0; it < 64; ++it) {
-        float2 acc = make_float2(0.f, 0.f);
+        float3 acc = make_float3(0.f, 0.f, 0.f);
         for (int p = threadIdx.x; p < np; p += blockDim.x) {
-            const float2 v = gauss_moment<E>(s_mu[p], s_sg[p], tau);
+            const float3 v = gauss_moment<E>(s_mu[p], s_sg[p], tau);
             acc.x = fmaf(s_n[p], v.x, acc.x);
             acc.y = fmaf(s_n[p], v.y, acc.y);
+            acc.z = fmaf(s_n[p], v.z, acc.z);
         }
-        acc = block_sum2(acc, fred);
-        const float F = acc.x - 1.f, dF = acc.y;
+        acc = block_sum3(acc, fred);
+        const float F = acc.x - 1.f, dF = acc.y, H = acc.z;
         if (F == 0.f) break;                       // tau is the root
         if (F > 0.f) lo = tau; else hi = tau;
-        const float tol = 1e-7f * fmaxf(1.f, fabsf(tau));
+        // tau's resolution: 1e-7 relative, but never below two units in the
+        // last place of tau (with a finer bound, a root just above a power of
+        // two leaves tau stepping between neighbouring floats)
+        const float at = fabsf(tau);
+        const float ulp = __int_as_float(__float_as_int(at) & 0x7f800000) * 1.1920929e-7f;
+        const float tol = fmaxf(1e-7f * fmaxf(1.f, at), 2.f * ulp);
+        if (hi - lo <= tol) break;                 // bracketed to that resolution
         if (dF > 0.f) {
-            const float nxt = tau + F / dF;
+            // Halley's step; Newton's (never past the root from the left)
+            // where the curvature term would turn it round
+            const float den = 2.f * dF * dF - F * H;
+            const float nxt = den > 0.f ? tau + 2.f * F * dF / den : tau + F / dF;
             if (fabsf(nxt - tau) <= tol) {         // converged (to fp32 resolution)
                 if (nxt > lo && nxt < hi) tau = nxt;
                 break;
@@ -398,7 +430,6 @@ select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float 
             if (nxt > lo && nxt < hi) { tau = nxt; continue; }
         }
         if (hi < INFINITY) {
-            if (hi - lo <= tol) break;
             tau = 0.5f * (lo + hi);                // safeguard: bisect the bracket
         } else {
             tau = lo + fmaxf(1.f, 2.f * (lo - (mu_max - 1.f)));   // no upper end yet: expand

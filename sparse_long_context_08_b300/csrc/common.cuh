@@ -117,6 +117,18 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
     v.y = warp_sum(v.y);
     return v;
 }
+// Block-wide sum of a float3; `red` >= 32 float4.
+__device__ __forceinline__ float3 block_sum3(float3 v, float4* red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v.x = warp_sum(v.x);
+    v.y = warp_sum(v.y);
+    v.z = warp_sum(v.z);
+    __syncthreads();
+    if (lane == 0) red[wid] = make_float4(v.x, v.y, v.z, 0.f);
+    __syncthreads();
+    const float4 r = lane < nw ? red[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    return make_float3(warp_sum(r.x), warp_sum(r.y), warp_sum(r.z));
+}
 __device__ __forceinline__ int block_sum_i(int v, int* red) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
     v = warp_sum_i(v);

@@ -661,6 +661,163 @@ __device__ __forceinline__ float pow_e(float a, int E, float ex) {
     return E == 2 ? a * a : (E == 1 ? a : powf(a, ex));
 }
 
+// One step of the threshold solve f(t) = sum_i (x_i - t)_+^e - 1 = 0, x
+// relative to the max, on the bracket lo <= t < hi with f(lo) >= 0 > f(hi)
+// (initially [-1, 0]: the max alone gives f(-1) >= 0, and f(0) = -1).  f is
+// convex and decreasing; d = -f'(t), h = f''(t) (e = 2: 2 #{x_i > t}; e = 1:
+// 0, where Halley's step is Newton's).  Left of the root the step is
+// Halley's, right of it Newton's (the tangent of a convex f meets 0 left of
+// the root), and a step that leaves the bracket bisects it.  Returns true once
+// t is the root to 1e-7, at least one unit in the last place on [-1, 0].
+__device__ __forceinline__ bool threshold_step(float f, float d, float h, float& t, float& lo,
+                                               float& hi) {
+    if (f >= 0.f) lo = t; else hi = t;
+    float nxt = lo;                                // no slope: bisect
+    if (d > 0.f) {
+        const float den = 2.f * d * d - f * h;
+        const float step = f > 0.f && den > 0.f ? 2.f * f * d / den : f / d;
+        nxt = t + step;
+        if (fabsf(step) <= 1e-7f) {
+            if (nxt > lo && nxt < hi) t = nxt;
+            return true;
+        }
+    }
+    if (hi - lo <= 1e-7f) return true;
+    t = nxt > lo && nxt < hi ? nxt : 0.5f * (lo + hi);
+    return false;
+}
+
+// The threshold t of the m candidates x (relative to the max; e = 1, 2) by
+// threshold_step, every thread of the block taking part.
+template <int E, bool kGlobal>
+__device__ float solve_threshold(const float* x, int m, float4* red) {
+    float t = -1.f, lo = -1.f, hi = 0.f;
+    for (int it = 0; it < 64; ++it) {
+        float3 acc = make_float3(0.f, 0.f, 0.f);
+        for (int i = threadIdx.x; i < m; i += blockDim.x) {
+            const float a = (kGlobal ? __ldcg(x + i) : x[i]) - t;
+            if (a > 0.f) {
+                if (E == 2) { acc.x = fmaf(a, a, acc.x); acc.y += a; acc.z += 1.f; }
+                else { acc.x += a; acc.y += 1.f; }
+            }
+        }
+        acc = block_sum3(acc, red);
+        if (threshold_step(acc.x - 1.f, E == 2 ? 2.f * acc.y : acc.y, E == 2 ? 2.f * acc.z : 0.f,
+                           t, lo, hi))
+            break;
+    }
+    return t;
+}
+
+// Weights w = (x - t)_+^e of the m candidates, with the support compacted to
+// the front of each warp's contiguous segment of [0, m): x[] takes its
+// weights, pos[] keeps its score indices.  A warp writes an entry only at or
+// below one it has already read, so no second buffer is needed.  Marks the
+// support tokens in `vtok`, adds the weights to `wsum` and returns the warp's
+// support count (the same in every lane).
+template <int E>
+__device__ __forceinline__ int weigh_support(float* x, int* pos, int m, float t, float ex,
+                                             uint32_t* vtok, float& wsum) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int seg = (m + nw - 1) / nw;
+    const int s0 = min(m, wid * seg), s1 = min(m, s0 + seg);
+    int cnt = 0;
+    for (int i0 = s0; i0 < s1; i0 += 32) {
+        const int i = i0 + lane;
+        float w = 0.f;
+        int p = 0;
+        if (i < s1) {
+            const float a = x[i] - t;
+            if (a > 0.f) {
+                w = pow_e(a, E, ex);
+                p = pos[i];
+            }
+        }
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, w > 0.f);
+        __syncwarp();                          // the chunk is read before any write
+        if (w > 0.f) {
+            const int dst = s0 + cnt + __popc(bal & ((1u << lane) - 1u));
+            x[dst] = w;
+            pos[dst] = p;
+            wsum += w;
+            atomicOr(&vtok[p >> 5], 1u << (p & 31));
+        }
+        cnt += __popc(bal);
+    }
+    return cnt;
+}
+
+// Score index -> V row (-1 for a page without a block) of the warp's
+// compacted support entries; independent loads, one round trip per 128.
+__device__ __forceinline__ void resolve_support_rows(int* pos, int m, int cnt,
+                                                     const int* __restrict__ ublk, int P, int Hkv,
+                                                     int kvh) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int s0 = min(m, wid * ((m + nw - 1) / nw));
+#pragma unroll 4
+    for (int j = s0 + lane; j < s0 + cnt; j += 32) {
+        const int p = pos[j];
+        const int ui = p / P;
+        const int blk = __ldcg(ublk + ui);
+        pos[j] = blk >= 0 ? ((blk * Hkv + kvh) * P + (p - ui * P)) : -1;
+    }
+}
+
+// Index in the candidate arrays of support entry j (0 <= j < the support's
+// size), given the warps' support counts.
+__device__ __forceinline__ int support_index(int j, const int* wcnt, int m) {
+    const int nw = blockDim.x >> 5;
+    const int seg = (m + nw - 1) / nw;
+    int w = 0;
+    while (j >= wcnt[w]) { j -= wcnt[w]; ++w; }
+    return w * seg + j;
+}
+
+// sum_j w_j V[row_j] over the support (entries taken by row groups of LPR
+// lanes, kTpvgRows rows in flight per group), reduced across row groups into
+// s_red[0 .. D) by the caller.
+template <typename T, int D, int RG, bool kGlobal>
+__device__ __forceinline__ void accumulate_support_rows(const float* x, const int* pos, int m,
+                                                        int sup, const int* wcnt, const T* vbase,
+                                                        float* s_red) {
+    constexpr int EPC = Elem<T>::kPer16;
+    constexpr int LPR = D / EPC;
+    const int lr = threadIdx.x % LPR;
+    const int rg = threadIdx.x / LPR;
+    float acc[EPC];
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
+    for (int j0 = rg; j0 < sup; j0 += RG * kTpvgRows) {
+        float w[kTpvgRows];
+        int row[kTpvgRows];
+#pragma unroll
+        for (int k = 0; k < kTpvgRows; ++k) {
+            const int j = j0 + k * RG;
+            w[k] = 0.f;
+            row[k] = -1;
+            if (j < sup) {
+                const int i = support_index(j, wcnt, m);
+                w[k] = kGlobal ? __ldcg(x + i) : x[i];
+                row[k] = kGlobal ? __ldcg(pos + i) : pos[i];
+            }
+        }
+        uint4 r[kTpvgRows];
+#pragma unroll
+        for (int k = 0; k < kTpvgRows; ++k)
+            if (row[k] >= 0) r[k] = ld_nc_v4(vbase + (int64_t)row[k] * D + lr * EPC);
+#pragma unroll
+        for (int k = 0; k < kTpvgRows; ++k)
+            if (row[k] >= 0) {
+                float v[EPC];
+                Elem<T>::widen(r[k], v);
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc[e] = fmaf(w[k], v[e], acc[e]);
+            }
+    }
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) s_red[rg * D + lr * EPC + e] = acc[e];
+}
+
 template <typename T, int D, int E>   // E: 2 alpha = 1.5, 1 alpha = 2, 0 any other alpha
 __global__ void __launch_bounds__(kTpvThreads)
 tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
@@ -672,8 +829,9 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
     int* s_pos = reinterpret_cast<int*>(s_x + cand_cap);              // [cand_cap] score index, then V row
     float* s_red = reinterpret_cast<float*>(s_pos + cand_cap);        // [RG][D]
     __shared__ float fred[40];
-    __shared__ float2 f2red[32];
+    __shared__ float4 f4red[32];
     __shared__ int ired[40];
+    __shared__ int s_wcnt[32];
     __shared__ float s_t;
 
     const int G = L.G;
@@ -760,47 +918,30 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
                 const int i = j * 32 + lane;
                 xr[j] = i < m ? s_x[i] : -INFINITY;
             }
-            float tt = -1.f;
+            float tt = -1.f, lo = -1.f, hi = 0.f;
             for (int it = 0; it < 64; ++it) {
-                float s0 = 0.f, s1 = 0.f;
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const float a = xr[j] - tt;
                     if (a > 0.f) {
-                        if (E == 2) { s0 = fmaf(a, a, s0); s1 += a; }
+                        if (E == 2) { s0 = fmaf(a, a, s0); s1 += a; s2 += 1.f; }
                         else { s0 += a; s1 += 1.f; }
                     }
                 }
                 s0 = warp_sum(s0);
                 s1 = warp_sum(s1);
-                const float dv = E == 2 ? 2.f * s1 : s1;
-                if (!(dv > 0.f)) break;
-                const float step = (s0 - 1.f) / dv;
-                tt += step;
-                if (!(step > 1e-7f)) break;     // at the root to fp32 resolution
+                if (E == 2) s2 = warp_sum(s2);
+                if (threshold_step(s0 - 1.f, E == 2 ? 2.f * s1 : s1, E == 2 ? 2.f * s2 : 0.f, tt,
+                                   lo, hi))
+                    break;
             }
             if (lane == 0) s_t = tt;
         }
         __syncthreads();
         t = s_t;
     } else if (E != 0) {
-        t = -1.f;
-        for (int it = 0; it < 64; ++it) {
-            float2 acc = make_float2(0.f, 0.f);
-            for (int i = tid; i < m; i += blockDim.x) {
-                const float a = s_x[i] - t;
-                if (a > 0.f) {
-                    if (E == 2) { acc.x = fmaf(a, a, acc.x); acc.y += a; }
-                    else { acc.x += a; acc.y += 1.f; }
-                }
-            }
-            acc = block_sum2(acc, f2red);
-            const float dv = E == 2 ? 2.f * acc.y : acc.y;
-            if (!(dv > 0.f)) break;
-            const float step = (acc.x - 1.f) / dv;
-            t += step;
-            if (!(step > 1e-7f)) break;
-        }
+        t = solve_threshold<E, false>(s_x, m, f4red);
     } else {
         const float ex = 1.f / (alpha - 1.f);
         float lo = -1.f, hi = -powf(static_cast<float>(m), 1.f - alpha);
@@ -817,57 +958,17 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
         t = 0.5f * (lo + hi);
     }
 
-    // weights in place; the support's V rows (one round trip for the blocks)
+    // weights, the support compacted per warp, then its V rows
     const float ex = 1.f / (alpha - 1.f);
-    const T* vbase = static_cast<const T*>(kv.v);
-    int sup = 0;
     float wsum = 0.f;
-    for (int i = tid; i < m; i += blockDim.x) {
-        const float a = s_x[i] - t;
-        const float w = a > 0.f ? pow_e(a, E, ex) : 0.f;
-        s_x[i] = w;
-        if (w > 0.f) {
-            ++sup;
-            wsum += w;
-            const int pos = s_pos[i];
-            const int ui = pos / P;
-            const int blk = __ldcg(ws.union_blk + (int64_t)u * L.Umax + ui);
-            s_pos[i] = blk >= 0 ? ((blk * Hkv + kvh) * P + (pos - ui * P)) : -1;
-            atomicOr(&ws.vtok[(int64_t)u * L.nvw + (pos >> 5)], 1u << (pos & 31));
-        }
-    }
-    sup = block_sum_i(sup, ired);
-    wsum = block_sum(wsum, fred);      // includes a barrier: weights and rows are visible
-
-    const int lr = tid % LPR;
-    const int rg = tid / LPR;
-    float acc[EPC];
-#pragma unroll
-    for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
-    for (int i0 = rg; i0 < m; i0 += RG * kTpvgRows) {        // kTpvgRows V rows in flight
-        float w[kTpvgRows];
-        int row[kTpvgRows];
-#pragma unroll
-        for (int k = 0; k < kTpvgRows; ++k) {
-            const int i = i0 + k * RG;
-            w[k] = i < m ? s_x[i] : 0.f;
-            row[k] = i < m ? s_pos[i] : -1;
-        }
-        uint4 r[kTpvgRows];
-#pragma unroll
-        for (int k = 0; k < kTpvgRows; ++k)
-            if (w[k] > 0.f && row[k] >= 0) r[k] = ld_nc_v4(vbase + (int64_t)row[k] * D + lr * EPC);
-#pragma unroll
-        for (int k = 0; k < kTpvgRows; ++k)
-            if (w[k] > 0.f && row[k] >= 0) {
-                float x[EPC];
-                Elem<T>::widen(r[k], x);
-#pragma unroll
-                for (int e = 0; e < EPC; ++e) acc[e] = fmaf(w[k], x[e], acc[e]);
-            }
-    }
-#pragma unroll
-    for (int e = 0; e < EPC; ++e) s_red[rg * D + lr * EPC + e] = acc[e];
+    const int cnt = weigh_support<E>(s_x, s_pos, m, t, ex, ws.vtok + (int64_t)u * L.nvw, wsum);
+    resolve_support_rows(s_pos, m, cnt, ws.union_blk + (int64_t)u * L.Umax, P, Hkv, kvh);
+    if (lane == 0) s_wcnt[wid] = cnt;
+    wsum = block_sum(wsum, fred);      // includes a barrier: weights, rows and counts are visible
+    int sup = 0;
+    for (int w = 0; w < kTpvThreads / 32; ++w) sup += s_wcnt[w];
+    accumulate_support_rows<T, D, RG, false>(s_x, s_pos, m, sup, s_wcnt,
+                                             static_cast<const T*>(kv.v), s_red);
     __syncthreads();
     for (int d = tid; d < D; d += blockDim.x) {
         float o = 0.f;
@@ -913,8 +1014,9 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
     constexpr int RG = kTpvgThreads / LPR;     // row groups
     __shared__ float s_red[RG * D];
     __shared__ float fred[40];
-    __shared__ float2 f2red[32];
+    __shared__ float4 f4red[32];
     __shared__ int ired[40];
+    __shared__ int s_wcnt[32];
 
     const int G = L.G;
     const int Hkv = Hq / G;
@@ -995,23 +1097,7 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
     // threshold t (relative to the max): f(t) = sum (x - t)_+^e - 1 = 0
     float t;
     if (E != 0) {
-        t = -1.f;
-        for (int it = 0; it < 64; ++it) {
-            float2 acc = make_float2(0.f, 0.f);
-            for (int i = tid; i < m; i += blockDim.x) {
-                const float a = __ldcg(cx + i) - t;
-                if (a > 0.f) {
-                    if (E == 2) { acc.x = fmaf(a, a, acc.x); acc.y += a; }
-                    else { acc.x += a; acc.y += 1.f; }
-                }
-            }
-            acc = block_sum2(acc, f2red);
-            const float dv = E == 2 ? 2.f * acc.y : acc.y;
-            if (!(dv > 0.f)) break;
-            const float step = (acc.x - 1.f) / dv;
-            t += step;
-            if (!(step > 1e-7f)) break;
-        }
+        t = solve_threshold<E, true>(cx, m, f4red);
     } else {
         const float ex = 1.f / (alpha - 1.f);
         float lo = -1.f, hi = -powf(static_cast<float>(m), 1.f - alpha);
@@ -1028,57 +1114,18 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
         t = 0.5f * (lo + hi);
     }
 
-    // weights in place; V row of each support token
+    // weights, the support compacted per warp, then its V rows
     const float ex = 1.f / (alpha - 1.f);
-    const T* vbase = static_cast<const T*>(kv.v);
-    int sup = 0;
     float wsum = 0.f;
-    for (int i = tid; i < m; i += blockDim.x) {
-        const float a = cx[i] - t;
-        const float w = a > 0.f ? pow_e(a, E, ex) : 0.f;
-        cx[i] = w;
-        if (w > 0.f) {
-            ++sup;
-            wsum += w;
-            const int pos = cp[i];
-            const int ui = pos / P;
-            const int blk = __ldcg(ws.union_blk + (int64_t)u * L.Umax + ui);
-            cp[i] = blk >= 0 ? ((blk * Hkv + kvh) * P + (pos - ui * P)) : -1;
-            atomicOr(&ws.vtok[(int64_t)u * L.nvw + (pos >> 5)], 1u << (pos & 31));
-        }
-    }
-    sup = block_sum_i(sup, ired);
-    wsum = block_sum(wsum, fred);      // includes a barrier: weights and rows are visible
-
-    const int lr = tid % LPR;
-    const int rg = tid / LPR;
-    float acc[EPC];
-#pragma unroll
-    for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
-    for (int i0 = rg; i0 < m; i0 += RG * kTpvgRows) {
-        float w[kTpvgRows];
-        int row[kTpvgRows];
-#pragma unroll
-        for (int k = 0; k < kTpvgRows; ++k) {
-            const int i = i0 + k * RG;
-            w[k] = i < m ? __ldcg(cx + i) : 0.f;
-            row[k] = i < m ? __ldcg(cp + i) : -1;
-        }
-        uint4 r[kTpvgRows];
-#pragma unroll
-        for (int k = 0; k < kTpvgRows; ++k)
-            if (w[k] > 0.f && row[k] >= 0) r[k] = ld_nc_v4(vbase + (int64_t)row[k] * D + lr * EPC);
-#pragma unroll
-        for (int k = 0; k < kTpvgRows; ++k)
-            if (w[k] > 0.f && row[k] >= 0) {
-                float x[EPC];
-                Elem<T>::widen(r[k], x);
-#pragma unroll
-                for (int e = 0; e < EPC; ++e) acc[e] = fmaf(w[k], x[e], acc[e]);
-            }
-    }
-#pragma unroll
-    for (int e = 0; e < EPC; ++e) s_red[rg * D + lr * EPC + e] = acc[e];
+    const int cnt = weigh_support<E>(cx, cp, m, t, ex, ws.vtok + (int64_t)u * L.nvw, wsum);
+    resolve_support_rows(cp, m, cnt, ws.union_blk + (int64_t)u * L.Umax, P, Hkv, kvh);
+    if ((tid & 31) == 0) s_wcnt[tid >> 5] = cnt;
+    __syncthreads();                   // (global) weights and rows visible to the block
+    wsum = block_sum(wsum, fred);
+    int sup = 0;
+    for (int w = 0; w < kTpvgThreads / 32; ++w) sup += s_wcnt[w];
+    accumulate_support_rows<T, D, RG, true>(cx, cp, m, sup, s_wcnt, static_cast<const T*>(kv.v),
+                                            s_red);
     __syncthreads();
     for (int d = tid; d < D; d += blockDim.x) {
         float o = 0.f;

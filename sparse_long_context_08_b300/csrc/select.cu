@@ -335,19 +335,6 @@ __device__ __forceinline__ float3 gauss_moment(float mu, float sig, float tau) {
     return make_float3(m1, Phi, phi / sig);
 }
 
-// Block-wide sum of a float3; `red` >= 32 float4.  Every thread calls it.
-__device__ __forceinline__ float3 block_sum3(float3 v, float4* red) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-    v.x = warp_sum(v.x);
-    v.y = warp_sum(v.y);
-    v.z = warp_sum(v.z);
-    __syncthreads();
-    if (lane == 0) red[wid] = make_float4(v.x, v.y, v.z, 0.f);
-    __syncthreads();
-    const float4 r = lane < nw ? red[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-    return make_float3(warp_sum(r.x), warp_sum(r.y), warp_sum(r.z));
-}
-
 template <int E>
 __global__ void __launch_bounds__(kSelThreads, 2)
 select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float alpha,

@@ -317,7 +317,7 @@ def test_discarded_mass_full_size_sampled_heads():
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (8, 1)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (8, 1), (16, 4), (32, 4), (64, 8)])
 def test_shapes(d, dtype, hq, hkv):
     w = make_workload("long128k", batch=2, seq_lens=[3000, 2049], head_dim=d, dtype=dtype,
                       num_q_heads=hq, num_kv_heads=hkv, page_size=16, budget_tokens=512,

@@ -13,6 +13,7 @@
 // keeps pages whose (alpha-1) * estimated max clears tau-hat - delta, and caps
 // the kept set by estimated-max rank with the same radix select.
 #include "common.cuh"
+#include "mills_ratio.h"
 
 EKV_DEFINE_STATUS(select)
 
@@ -312,6 +313,25 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     }
 }
 
+// Phi(u) and phi(u) of the standard normal from one exponential: the tail
+// Phi(-x) = phi(x) R(x), x = |u|, with R the Mills ratio in the rational form
+// t P(t), t = 1 / (1 + x / 4) (coefficients fitted by gen_mills_ratio.py;
+// fp32 relative error of R below 6e-7).  phi's argument -x^2 / 2 is taken
+// with its rounding error (x^2 = x2 + x2e exactly), so phi keeps expf's
+// accuracy for large x.
+__device__ __forceinline__ float2 normal_cdf_pdf(float u) {
+    const float x = fabsf(u);
+    const float x2 = x * x;
+    const float x2e = fmaf(x, x, -x2);
+    const float phi = 0.398942280f * expf(-0.5f * x2) * fmaf(-0.5f, x2e, 1.f);
+    const float t = __fdividef(1.f, fmaf(kMillsMap, x, 1.f));
+    float p = kMillsP[kMillsDegree];
+#pragma unroll
+    for (int i = kMillsDegree - 1; i >= 0; --i) p = fmaf(p, t, kMillsP[i]);
+    const float tail = phi * (t * p);
+    return make_float2(u < 0.f ? tail : 1.f - tail, phi);
+}
+
 // E[(Y - tau)_+^e] and its derivative magnitude -dE/dtau for Y ~ N(mu, sig^2):
 //   e = 2: E = (a^2 + sig^2) Phi(u) + a sig phi(u),   -dE = 2 (a Phi(u) + sig phi(u))
 //   e = 1: E = a Phi(u) + sig phi(u),                  -dE = Phi(u)
@@ -327,8 +347,8 @@ __device__ __forceinline__ float3 gauss_moment(float mu, float sig, float tau) {
                       : make_float3(ap, a > 0.f ? 1.f : 0.f, 0.f);
     }
     const float u = a / sig;
-    const float Phi = 0.5f * erfcf(-u * 0.70710678118654752f);
-    const float phi = 0.39894228040143268f * expf(-0.5f * u * u);
+    const float2 cp = normal_cdf_pdf(u);
+    const float Phi = cp.x, phi = cp.y;
     const float m1 = fmaf(a, Phi, sig * phi);
     if (E == 2)
         return make_float3(fmaf(fmaf(a, a, sig * sig), Phi, a * sig * phi), 2.f * m1, 2.f * Phi);

@@ -3,7 +3,11 @@
 //   bbox:  U_p = s * sum_j max(q_j kmin_j, q_j kmax_j)   (upper bound on s q.k)
 //   gauss: m_p = s q.mean_p,  s_p = s sqrt(sum_j q_j^2 var_pj)
 //
-// HBM-bound streaming kernel.  The valid pages of all sequences, in
+// Two kernels.  bf16 metadata with 4 or 8 kv heads takes the bbox bound on
+// the tensor cores (score_bbox_tc_kernel, described where it is defined).
+// Every other case -- fp32 metadata, the Gaussian statistics, other head
+// layouts -- takes score_kernel, an HBM-bound streaming kernel on the CUDA
+// cores.  Its valid pages of all sequences, in
 // (sequence, logical page) order, are cut into one contiguous range per CTA;
 // the CTA stages the range's page-table entries in shared memory.  A warp owns
 // one kv head (and a part of the range) at a time: LPR lanes per page row,

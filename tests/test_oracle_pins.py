@@ -605,3 +605,64 @@ def test_gauss_meta_statistics_match_token_scores(oracle_lib):
             z = float(w.scale) * K[w.page_table[0, p], 0, :n, 0] * float(w.q[0, h, 0])
             assert abs(m[h, p] - z.mean()) < 1e-12
             assert abs(s[h, p] - z.std()) < 1e-12
+
+
+def _uncorrelated_pages(w, seed=5):
+    """Overwrite every page of a one-kv-head fp32 workload with keys whose
+    coordinates are exactly uncorrelated over the page's tokens: coordinate j
+    of token t is c_j + a_j H[t, j + 1], with H a Sylvester-Hadamard matrix of
+    the page's order (rows shuffled per page).  Its columns other than the
+    first are +-1 vectors with zero mean and mutually orthogonal, so each
+    coordinate has mean c_j and population variance a_j^2, and the sample
+    covariance of two coordinates is exactly 0.  c and a are dyadic, so every
+    key is exact in fp32.  Returns the per-block (c, a)."""
+    from scipy.linalg import hadamard
+    P, d = w.page_size, w.head_dim
+    H = hadamard(P).astype(np.float64)
+    rng = np.random.default_rng(seed)
+    ca = {}
+    for blk in range(w.num_blocks):
+        c = np.array([0.125 * ((3 * j + blk) % 7 - 3) for j in range(d)])
+        a = np.array([0.25 * (1 + (j + 2 * blk) % 5) for j in range(d)])
+        rows = H[rng.permutation(P)]
+        w.k_pool[blk, 0] = (c[None, :] + a[None, :] * rows[:, 1:d + 1]).astype(np.float32)
+        ca[blk] = (c, a)
+    return ca
+
+
+def test_gauss_meta_statistics_match_token_scores_multidim(oracle_lib):
+    """[EntmaxKV] §2.A, Gaussian page statistics at d = 12: on pages whose
+    coordinates are exactly uncorrelated, the diagonal model is exact, so m_p
+    and s_p must equal numpy's mean and population std of the token scores
+    s q.k_t.  The same check rejects the two plausible slips of the spread: the
+    sum of per-coordinate standard deviations s sum_j |q_j| sd_j, and q_j not
+    squared."""
+    w = make_workload("gauss64k", batch=1, num_q_heads=3, num_kv_heads=1, head_dim=12,
+                      page_size=16, seq_lens=[16 * 6], context=96, dtype="f32", flat_heads=(),
+                      planted_pages=0, seed=21)
+    ca = _uncorrelated_pages(w)
+    kv = oracle.KV(w)
+    meta = oracle.build_meta(kv)
+    m, s = oracle.score_gauss(kv, meta, float(w.scale))
+    K = w.k_pool.astype(np.float64)
+    sc = float(w.scale)
+    for blk, (c, a) in ca.items():          # the metadata itself is exact here
+        np.testing.assert_allclose(meta.mean[blk, 0], c, rtol=0, atol=1e-15)
+        np.testing.assert_allclose(meta.var[blk, 0], a * a, rtol=0, atol=1e-15)
+    checked = 0
+    for h in range(w.num_q_heads):
+        qh = w.q[0, h].astype(np.float64)
+        for p in range(w.pages_of(0)):
+            blk = w.page_table[0, p]
+            z = sc * (K[blk, 0] @ qh)
+            scale_z = sc * (np.abs(qh) @ (np.abs(ca[blk][0]) + ca[blk][1]))
+            assert abs(m[h, p] - z.mean()) <= 1e-12 * scale_z
+            assert abs(s[h, p] - z.std()) <= 1e-12 * scale_z
+            # the slips this pins: each misses numpy's std by far more than 1e-12
+            sd = np.sqrt(meta.var[blk, 0])
+            sum_of_sd = sc * (np.abs(qh) @ sd)
+            unsquared_q = sc * np.sqrt(np.abs(qh) @ meta.var[blk, 0])
+            assert abs(sum_of_sd - z.std()) > 1e-3 * z.std()
+            assert abs(unsquared_q - z.std()) > 1e-3 * z.std()
+            checked += 1
+    assert checked == w.num_q_heads * 6

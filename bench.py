@@ -40,6 +40,14 @@ FALLBACK_HBM_GBS = 6400.0
 KERNELS_PER_STEP = 5   # score, select, plan, qk, tpv (threshold + values)
 
 
+def kernels_per_step(w) -> int:
+    """Kernel launches of one step: score, select, plan, qk, tpv -- without the
+    plan where the top-k selection builds the page union itself (per-head or
+    shared top-k over at most 4096 pages per sequence: one CTA per selection)."""
+    planned = w.policy in ("topk", "topk_shared") and w.max_pages <= 4096
+    return KERNELS_PER_STEP - (1 if planned else 0)
+
+
 def parse():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -210,6 +218,27 @@ def measured_traffic(kernel: str, units: int):
         return int(round(float(k["bytes_per_unit"]) * units))
     except (OSError, KeyError, ValueError):
         return None
+
+
+def timed_replays(graph, k: int, flush_l2) -> list[float]:
+    """Device time (ms) of k replays of `graph`, each behind an L2 flush.
+
+    Every replay is enqueued right behind the previous flush, with no host
+    synchronisation in between, so the GPU is still busy flushing when the
+    start event and the graph's kernels are enqueued: the events bracket the
+    step's execution on the device, not the host's launch latency (which the
+    end-to-end figure carries)."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+    flush_l2(0)
+    for i in range(k):
+        starts[i].record()
+        graph.replay()
+        ends[i].record()
+        flush_l2(i + 7)                    # the next step's flush, enqueued behind this one
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
 
 
 # ---------------------------------------------------------------------------
@@ -387,9 +416,8 @@ def run_ours(args):
         evs[0].record()
         dec.score(q)
         evs[1].record()
-        dec.select()
         E.entmaxkv_set_stage_events(evs[2:6])
-        dec.decode(q)
+        dec.select_decode(q)            # select | plan (inside select when it builds the union) | qk | tpv
         E.entmaxkv_set_stage_events(None)
     torch.cuda.synchronize()
 
@@ -404,26 +432,17 @@ def run_ours(args):
     K = args.steps
     names = ["score", "select", "plan", "qk", "tpv"]
     stage = {n: [] for n in names}
-    total = []
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(bus_id_of(local_rank)) if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
     torch.cuda.synchronize()
-    for i in range(K):
-        t_start.record()
-        graph.replay()
-        t_end.record()
-        torch.cuda.synchronize()
-        total.append(t_start.elapsed_time(t_end))
-        flush_l2(i + 7)                     # L2 flush between steps, outside the events
+    total = timed_replays(graph, K, flush_l2)
     for i in range(min(K, 100)):
+        flush_l2(i + 3)                     # keeps the GPU busy while the replay is enqueued
         staged.replay()
         torch.cuda.synchronize()
         t = [evs[j].elapsed_time(evs[j + 1]) for j in range(5)]
         for n_, v in zip(names, t):
             stage[n_].append(v)
-        flush_l2(i + 3)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     ms_per_step = max_over_ranks(sum(total), world, "cuda") / K
@@ -503,7 +522,7 @@ def run_ours(args):
                             "union_pages": int(up.sum()), "v_rows": int(vr.sum())},
         "stage_us": {n: v * 1e3 for n, v in mean.items()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": KERNELS_PER_STEP * K, "clocks": clocks,
+        "gpu_launches": kernels_per_step(w) * K, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -587,25 +606,16 @@ def run_full(args):
     K = args.steps
     names = [n for n, _ in pre] + dnames
     stage = {n: [] for n in names}
-    total = []
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(bus_id_of(local_rank)) if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
     torch.cuda.synchronize()
-    for i in range(K):
-        t_start.record()
-        graph.replay()
-        t_end.record()
-        torch.cuda.synchronize()
-        total.append(t_start.elapsed_time(t_end))
-        flush_l2(i + 7)
+    total = timed_replays(graph, K, flush_l2)
     for i in range(min(K, 50)):
+        flush_l2(i + 3)
         staged.replay()
         torch.cuda.synchronize()
         for j, n_ in enumerate(names):
             stage[n_].append(evs[j].elapsed_time(evs[j + 1]))
-        flush_l2(i + 3)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     ms_per_step = max_over_ranks(sum(total), world, "cuda") / K

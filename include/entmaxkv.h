@@ -25,7 +25,10 @@
  *   EKV_CUDA_ERROR.  Malformed DEVICE data (a page-table entry outside
  *   [0, num_blocks), a selected page outside a sequence) is skipped by the
  *   kernels and recorded in a sticky per-device word read with
- *   entmaxkv_read_device_status.
+ *   entmaxkv_read_device_status.  Every wait inside a kernel (on an mbarrier
+ *   that copies or other warps complete) is bounded by 2 s of %globaltimer; a
+ *   wait that runs out stops the kernel's work, records a timeout in the same
+ *   word and the kernel returns, so the context stays usable.
  * - Supported shapes: head_dim 64 or 128; page_size 16 or 32; num_q_heads a
  *   multiple of num_kv_heads with group size 1, 2, 4 or 8; K/V fp32 or bf16.
  * - Layouts (row-major, contiguous):
@@ -56,7 +59,8 @@ typedef enum {
     EKV_UNSUPPORTED = 2,          /* valid but outside the supported shapes  */
     EKV_WORKSPACE_TOO_SMALL = 3,
     EKV_CUDA_ERROR = 4,           /* a CUDA launch or query failed           */
-    EKV_DEVICE_CHECK_FAILED = 5   /* the kernels met malformed device data   */
+    EKV_DEVICE_CHECK_FAILED = 5,  /* the kernels met malformed device data   */
+    EKV_DEVICE_TIMEOUT = 6        /* a bounded wait inside a kernel gave up  */
 } ekv_status;
 
 typedef enum { EKV_F32 = 0, EKV_BF16 = 1 } ekv_dtype;
@@ -162,6 +166,23 @@ int entmaxkv_decode(const float* q, int32_t num_q_heads, float scale,
                     float* out, float* tau_out, int32_t* support_out,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* Stages 3 and 4 in one call [EntmaxKV §2.B, §2.C]: entmaxkv_select then
+ * entmaxkv_decode on that selection, with the same results (sel, n_sel and aux
+ * are written as entmaxkv_select writes them; out, tau_out and support_out as
+ * entmaxkv_decode).  cap_pages = budget_tokens / page_size.  For the top-k
+ * policies the selection kernel also builds, in the workspace, the union of
+ * each kv head's selected pages that the decode reads (the G query heads of a
+ * kv head select as one thread-block cluster), so the decode does not rebuild
+ * it.  Arguments and checks as the two calls; workspace: at least
+ * entmaxkv_workspace_size(..., cap_pages) bytes, 256-byte aligned, not shared
+ * with a concurrent call. */
+int entmaxkv_select_decode(const float* page_scores, const float* q, int32_t num_q_heads,
+                           float scale, const ekv_paged_kv* kv, int32_t policy,
+                           int32_t budget_tokens, float alpha, float delta, int32_t* sel,
+                           int32_t* n_sel, float* aux, float* out, float* tau_out,
+                           int32_t* support_out, void* workspace, size_t ws_bytes,
+                           void* stream);
+
 /* Full-cache alpha-entmax decode, the exact attention the sparse decode
  * approximates ([EntmaxKV] §1 and §3: sparse output equals it whenever the
  * kept pages hold its support).  For each (b, h): every valid token of
@@ -263,10 +284,22 @@ size_t entmaxkv_workspace_size(int32_t batch, int32_t num_q_heads,
 /* Host-only: a static string naming an ekv_status value. */
 const char* entmaxkv_status_string(int32_t status);
 
-/* Reads (and clears) the sticky device-data check word of the current device:
- * *status_out = EKV_OK or EKV_DEVICE_CHECK_FAILED.  Synchronises `stream`.
- * Returns EKV_CUDA_ERROR if the copy fails. */
+/* Reads (and clears) the sticky device status word of the current device:
+ * *status_out = EKV_DEVICE_TIMEOUT if a bounded wait gave up since the last
+ * read (this takes precedence), else EKV_DEVICE_CHECK_FAILED if a kernel met
+ * malformed device data, else EKV_OK.  Synchronises `stream`.  Returns
+ * EKV_CUDA_ERROR if the copy fails. */
 int entmaxkv_read_device_status(int32_t* status_out /* host */, void* stream);
+
+/* Self-check of the bounded-wait give-up path (the page has no counterpart;
+ * it is a health check for this library).  Launches one single-warp kernel on
+ * `stream` that waits on an mbarrier whose phase can never complete, with a
+ * limit of limit_us microseconds (1 .. 100000) instead of the kernels' 2 s.
+ * The wait runs out, the kernel records a timeout exactly as the score, q.k
+ * and softmax kernels do, and returns: the next entmaxkv_read_device_status
+ * reports EKV_DEVICE_TIMEOUT.  No memory is copied and nothing waits on the
+ * kernel.  Returns EKV_INVALID_ARG for a limit outside the range. */
+int entmaxkv_check_wait_timeout(uint32_t limit_us, void* stream);
 
 /* Measurement aid (not part of the method): record four caller-created
  * cudaEvent_t handles around the kernels of every later entmaxkv_decode call on

@@ -111,11 +111,19 @@ class EntmaxKVDecoder(_HostStepGraphs):
                           self.alpha, self.out, self.tau, self.support, self.workspace, stream)
         return self.out
 
+    def select_decode(self, q: torch.Tensor, stream=None) -> torch.Tensor:
+        """select then decode in one library call (the selection also builds
+        the decode's page union); the same results as select() and decode()."""
+        E.entmaxkv_select_decode(self.page_scores, q, self.Hq, self.scale, self.kv, self.policy,
+                                 self.budget, self.alpha, self.delta, self.sel, self.n_sel,
+                                 self.aux, self.out, self.tau, self.support, self.workspace,
+                                 stream)
+        return self.out
+
     def step(self, q: torch.Tensor, stream=None) -> torch.Tensor:
         """One decode step for device-resident q [B, Hq, d]; returns `out` (device)."""
         self.score(q, stream)
-        self.select(stream)
-        return self.decode(q, stream)
+        return self.select_decode(q, stream)
 
     def _step_host_eager(self, q_host, out_host, q_dev, s) -> None:
         with torch.cuda.stream(s):

@@ -42,9 +42,11 @@ KV to_kv(const ekv_paged_kv* kv) {
               kv->head_dim, kv->page_table, kv->max_pages, kv->seq_lens, kv->batch};
 }
 
+// The launchers report a shape outside what the kernels support with
+// ekv::kShapeUnsupported; any other error came from CUDA itself.
 int from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return EKV_OK;
-    if (e == cudaErrorInvalidValue) return EKV_UNSUPPORTED;
+    if (e == ekv::kShapeUnsupported) return EKV_UNSUPPORTED;
     return EKV_CUDA_ERROR;
 }
 
@@ -64,6 +66,7 @@ const char* entmaxkv_status_string(int32_t s) {
         case EKV_WORKSPACE_TOO_SMALL: return "workspace too small";
         case EKV_CUDA_ERROR: return "CUDA error";
         case EKV_DEVICE_CHECK_FAILED: return "malformed device data (page table or selection)";
+        case EKV_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up (device timeout)";
         default: return "unknown status";
     }
 }
@@ -145,10 +148,11 @@ int entmaxkv_select(const float* page_scores, const ekv_paged_kv* kv, int32_t nu
     return EKV_INVALID_ARG;
 }
 
-static int decode_impl(const float* q, int32_t num_q_heads, float scale, const ekv_paged_kv* kv,
-                       const int32_t* sel, const int32_t* n_sel, int32_t cap_pages, float alpha,
-                       float* out, float* tau_out, int32_t* support_out, void* workspace,
-                       size_t ws_bytes, void* stream) {
+// Checks of a decode call's arguments; on success *L is its workspace layout.
+static int check_decode(const float* q, int32_t num_q_heads, float scale, const ekv_paged_kv* kv,
+                        const int32_t* sel, const int32_t* n_sel, int32_t cap_pages, float alpha,
+                        const float* out, const void* workspace, size_t ws_bytes,
+                        ekv::DecodeLayout* L) {
     int st = check_kv(kv, true, true);
     if (st) return st;
     if ((st = check_heads(kv, num_q_heads))) return st;
@@ -158,10 +162,20 @@ static int decode_impl(const float* q, int32_t num_q_heads, float scale, const e
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EKV_INVALID_ARG;
     if ((int64_t)kv->max_pages > ekv::kMaxPagesTopk) return EKV_UNSUPPORTED;
     if ((int64_t)kv->num_blocks * kv->num_kv_heads * kv->page_size > INT32_MAX) return EKV_UNSUPPORTED;
-    const ekv::DecodeLayout L = ekv::decode_layout(kv->batch, num_q_heads, kv->num_kv_heads,
-                                                   kv->head_dim, kv->page_size, kv->max_pages,
-                                                   cap_pages);
-    if (ws_bytes < L.total) return EKV_WORKSPACE_TOO_SMALL;
+    *L = ekv::decode_layout(kv->batch, num_q_heads, kv->num_kv_heads, kv->head_dim,
+                            kv->page_size, kv->max_pages, cap_pages);
+    if (ws_bytes < L->total) return EKV_WORKSPACE_TOO_SMALL;
+    return EKV_OK;
+}
+
+static int decode_impl(const float* q, int32_t num_q_heads, float scale, const ekv_paged_kv* kv,
+                       const int32_t* sel, const int32_t* n_sel, int32_t cap_pages, float alpha,
+                       float* out, float* tau_out, int32_t* support_out, void* workspace,
+                       size_t ws_bytes, void* stream) {
+    ekv::DecodeLayout L;
+    const int st = check_decode(q, num_q_heads, scale, kv, sel, n_sel, cap_pages, alpha, out,
+                                workspace, ws_bytes, &L);
+    if (st) return st;
     return from_cuda(ekv::launch_decode(q, num_q_heads, scale, to_kv(kv), sel, n_sel, cap_pages,
                                         alpha, out, tau_out, support_out, workspace, L,
                                         static_cast<cudaStream_t>(stream)));
@@ -173,6 +187,40 @@ int entmaxkv_decode(const float* q, int32_t num_q_heads, float scale, const ekv_
                     size_t ws_bytes, void* stream) {
     return decode_impl(q, num_q_heads, scale, kv, sel, n_sel, cap_pages, alpha, out, tau_out,
                        support_out, workspace, ws_bytes, stream);
+}
+
+int entmaxkv_select_decode(const float* page_scores, const float* q, int32_t num_q_heads,
+                           float scale, const ekv_paged_kv* kv, int32_t policy,
+                           int32_t budget_tokens, float alpha, float delta, int32_t* sel,
+                           int32_t* n_sel, float* aux, float* out, float* tau_out,
+                           int32_t* support_out, void* workspace, size_t ws_bytes,
+                           void* stream) {
+    if (!kv || !page_scores) return EKV_INVALID_ARG;
+    if (budget_tokens <= 0 || kv->page_size <= 0 || budget_tokens / kv->page_size < 1)
+        return EKV_INVALID_ARG;
+    const int cap = budget_tokens / kv->page_size;
+    ekv::DecodeLayout L;
+    int st = check_decode(q, num_q_heads, scale, kv, sel, n_sel, cap, alpha, out, workspace,
+                          ws_bytes, &L);
+    if (st) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool planned = false;
+    cudaError_t e;
+    if (policy == EKV_SELECT_TOPK || policy == EKV_SELECT_TOPK_SHARED) {
+        e = ekv::launch_select_topk(page_scores, to_kv(kv), num_q_heads, cap, sel, n_sel, aux,
+                                    policy == EKV_SELECT_TOPK_SHARED, s, workspace, &L, &planned);
+    } else if (policy == EKV_SELECT_GAUSS) {
+        if (!std::isfinite(delta)) return EKV_INVALID_ARG;
+        if (std::fabs(alpha - 1.5f) > 1e-6f && std::fabs(alpha - 2.f) > 1e-6f) return EKV_UNSUPPORTED;
+        if (kv->max_pages > ekv::kMaxPagesGauss) return EKV_UNSUPPORTED;
+        e = ekv::launch_select_gauss(page_scores, to_kv(kv), num_q_heads, cap, alpha, delta, sel,
+                                     n_sel, aux, s);
+    } else {
+        return EKV_INVALID_ARG;
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(ekv::launch_decode(q, num_q_heads, scale, to_kv(kv), sel, n_sel, cap, alpha,
+                                        out, tau_out, support_out, workspace, L, s, planned));
 }
 
 size_t entmaxkv_full_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
@@ -290,9 +338,16 @@ int entmaxkv_read_device_status(int32_t* status_out, void* stream) {
     if (e == cudaSuccess) e = ekv::take_status_score(&flag, s);
     if (e == cudaSuccess) e = ekv::take_status_select(&flag, s);
     if (e == cudaSuccess) e = ekv::take_status_decode(&flag, s);
+    if (e == cudaSuccess) e = ekv::take_status_selfcheck(&flag, s);
     if (e != cudaSuccess) return EKV_CUDA_ERROR;
-    *status_out = flag ? EKV_DEVICE_CHECK_FAILED : EKV_OK;
+    *status_out = (flag & 2) ? EKV_DEVICE_TIMEOUT : (flag & 1) ? EKV_DEVICE_CHECK_FAILED : EKV_OK;
     return EKV_OK;
+}
+
+int entmaxkv_check_wait_timeout(uint32_t limit_us, void* stream) {
+    if (limit_us == 0 || limit_us > 100000u) return EKV_INVALID_ARG;
+    return from_cuda(ekv::launch_wait_timeout_check((uint64_t)limit_us * 1000u,
+                                                    static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -254,16 +254,19 @@ __device__ __forceinline__ uint64_t global_ns() {
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
-// Waits for the phase with the given parity; gives up after kWaitLimitNs and
-// returns false (the caller records an error and stops issuing work).
+// Waits for the phase with the given parity; gives up after limit_ns and
+// returns false (the caller records a timeout and stops issuing work).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 // Global -> shared bulk copy, completion signalled on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned).

@@ -101,8 +101,9 @@ plan_kernel(KV kv, int Hq, const int32_t* __restrict__ sel, const int32_t* __res
     __shared__ int red[40];
     __shared__ int s_ns[G];
     const int nwm = (kv.maxp + 31) / 32;
-    build_plan<G>(kv, Hq, sel, n_sel, cap, ws, L, blockIdx.x, s_plan,
-                  reinterpret_cast<int*>(s_plan + (size_t)G * nwm), red, s_ns);
+    int* s_upage = reinterpret_cast<int*>(s_plan + (size_t)G * nwm);
+    build_plan<G>(kv, Hq, sel, n_sel, cap, ws, L, blockIdx.x, s_plan, s_upage, s_upage + L.Umax,
+                  red, s_ns);
 }
 
 // Plan of the full-cache decode: the union of unit u is every valid page of
@@ -260,7 +261,7 @@ qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, Decod
                 const int slot = k % nslots;
                 const int use = k / nslots;
                 if (use > 0 && !mbar_wait(&empty[slot], (uint32_t)((use - 1) & 1))) {
-                    flag_bad_data();      // a consumer stalled: hand over an empty page
+                    flag_timeout();      // a consumer stalled: hand over an empty page
                     valid = 0;
                 }
                 info[slot] = QkInfo{uu, ii, valid, mask};
@@ -303,7 +304,7 @@ qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, Decod
         const int slot = k % nslots;
         const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], (uint32_t)((k / nslots) & 1)));
         if (!ok) {
-            if (lane == 0) flag_bad_data();
+            if (lane == 0) flag_timeout();
             break;
         }
         const QkInfo in = info[slot];
@@ -362,7 +363,7 @@ qk_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, Decod
             float pm = -INFINITY;
             if ((in.mask >> lane) & 1)
                 for (int t = 0; t < in.valid; ++t) pm = fmaxf(pm, st[lane * P + t]);
-            ws.pmax[((int64_t)in.u * L.Umax + in.i) * G + lane] = pm;
+            ws.pmax[((int64_t)in.u * G + lane) * L.Umax + in.i] = pm;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
@@ -602,13 +603,13 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
         if constexpr (kPM) {
             pgm = fmaxf(pgm, __shfl_xor_sync(0xFFFFFFFFu, pgm, 1));
             pgm = fmaxf(pgm, __shfl_xor_sync(0xFFFFFFFFu, pgm, 2));
-            if (g < G && t == 0) ws.pmax[((int64_t)d.u * L.Umax + d.i) * G + g] = pgm;
+            if (g < G && t == 0) ws.pmax[((int64_t)d.u * G + g) * L.Umax + d.i] = pgm;
         }
         hm = fmaxf(hm, pgm);
         __syncwarp();        // every lane is done with stage st before it is refilled
     }
     if (failed) {
-        if (lane == 0) flag_bad_data();
+        if (lane == 0) flag_timeout();
         return;
     }
     {
@@ -628,9 +629,9 @@ constexpr int kTpvPmVec = 8;          // page maxima per thread per round trip
 // Union pages i < ucnt of a head whose largest z' exceeds max - 1 (only those
 // can hold a token with nonzero weight), written to list[] in a fixed thread
 // order; returns their count.  pm[] holds the first round of maxima (entries
-// j * blockDim + tid); later rounds are read from pmr (page i at pmr[i * G]).
+// j * blockDim + tid); later rounds are read from pmr (page i at pmr[i]).
 // Every thread calls it.
-__device__ int list_candidate_pages(float (&pm)[kTpvPmVec], const float* __restrict__ pmr, int G,
+__device__ int list_candidate_pages(float (&pm)[kTpvPmVec], const float* __restrict__ pmr,
                                     int ucnt, float mx, int* list, int* ired) {
     const int tid = threadIdx.x, nt = blockDim.x;
     int npl = 0;
@@ -639,7 +640,7 @@ __device__ int list_candidate_pages(float (&pm)[kTpvPmVec], const float* __restr
 #pragma unroll
             for (int j = 0; j < kTpvPmVec; ++j) {
                 const int i = p0 + j * nt + tid;
-                pm[j] = i < ucnt ? __ldcg(pmr + (int64_t)i * G) : -INFINITY;
+                pm[j] = i < ucnt ? __ldcg(pmr + i) : -INFINITY;
             }
         }
         int c = 0;
@@ -818,6 +819,64 @@ __device__ __forceinline__ void accumulate_support_rows(const float* x, const in
     for (int e = 0; e < EPC; ++e) s_red[rg * D + lr * EPC + e] = acc[e];
 }
 
+// Weights w = (x - t)_+^e of the m candidates of tpv_kernel, the support
+// compacted to the front of each warp's contiguous segment of [0, m) in place
+// (a warp writes an entry only at or below one it has already read): x[] takes
+// the weights and pos[] the V rows.  pos[] holds a candidate's index f into
+// the head's candidate pages (page f >> pshift of the list, token f & (P - 1)),
+// s_pl / s_pb those pages' union positions and physical blocks.  Marks the
+// support tokens in `vtok`, adds the weights to `wsum` and returns the warp's
+// support count (the same in every lane).
+template <int E>
+__device__ __forceinline__ int weigh_listed_support(float* x, int* pos, int m, float t, float ex,
+                                                    const int* s_pl, const int* s_pb, int pshift,
+                                                    int Hkv, int kvh, uint32_t* vtok,
+                                                    float& wsum) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int P = 1 << pshift;
+    const int seg = (m + nw - 1) / nw;
+    const int s0 = min(m, wid * seg), s1 = min(m, s0 + seg);
+    int cnt = 0;
+    for (int i0 = s0; i0 < s1; i0 += 32) {
+        const int i = i0 + lane;
+        float w = 0.f;
+        int row = -1, zi = 0;
+        if (i < s1) {
+            const float a = x[i] - t;
+            if (a > 0.f) {
+                w = pow_e(a, E, ex);
+                const int f = pos[i];
+                const int k = f >> pshift, tok = f & (P - 1);
+                const int blk = s_pb[k];
+                row = blk >= 0 ? (blk * Hkv + kvh) * P + tok : -1;
+                zi = (s_pl[k] << pshift) + tok;
+            }
+        }
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, w > 0.f);
+        __syncwarp();                          // the chunk is read before any write
+        if (w > 0.f) {
+            const int dst = s0 + cnt + __popc(bal & ((1u << lane) - 1u));
+            x[dst] = w;
+            pos[dst] = row;
+            wsum += w;
+            atomicOr(&vtok[zi >> 5], 1u << (zi & 31));
+        }
+        cnt += __popc(bal);
+    }
+    return cnt;
+}
+
+// Threshold and values, one CTA per head, from the per-page maxima qk wrote:
+//   1. one round trip for the union size and the head's pmax row: the head's
+//      max and the union pages whose maximum is above max - 1 -- only they can
+//      hold a token with nonzero weight, since tau >= max - 1;
+//   2. one round trip for those pages' scores and physical blocks; the
+//      candidates z' - max > -1 are compacted (fixed thread order);
+//   3. tau solves sum (z' - tau)_+^(1/(alpha-1)) = 1 by a safeguarded Halley
+//      iteration (alpha 1.5 and 2; one warp with the candidates in registers
+//      when there are at most 1024) or by bisection (other alpha);
+//   4. the weights, the support compacted per warp, and one round trip for its
+//      V rows only: out = sum p v / sum p.
 template <typename T, int D, int E>   // E: 2 alpha = 1.5, 1 alpha = 2, 0 any other alpha
 __global__ void __launch_bounds__(kTpvThreads)
 tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
@@ -826,8 +885,10 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
     constexpr int LPR = D / EPC;              // lanes per V row
     constexpr int RG = kTpvThreads / LPR;     // V rows per pass
     extern __shared__ __align__(16) float s_x[];                      // [cand_cap] x, then weights
-    int* s_pos = reinterpret_cast<int*>(s_x + cand_cap);              // [cand_cap] score index, then V row
+    int* s_pos = reinterpret_cast<int*>(s_x + cand_cap);              // [cand_cap] candidate, then V row
     float* s_red = reinterpret_cast<float*>(s_pos + cand_cap);        // [RG][D]
+    int* s_pl = reinterpret_cast<int*>(s_red + RG * D);               // [Umax] candidate pages
+    int* s_pb = s_pl + L.Umax;                                        // [Umax] their blocks
     __shared__ float fred[40];
     __shared__ float4 f4red[32];
     __shared__ int ired[40];
@@ -844,23 +905,29 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
     const int u = b * Hkv + kvh;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int P = kv.P;
-    const int zn = L.Umax * P;
-    const float* z = ws.z + ((int64_t)u * G + hg) * zn;
+    const int pshift = P == 32 ? 5 : 4;                               // page sizes are 16 or 32
+    const float* z = ws.z + ((int64_t)u * G + hg) * L.Umax * P;
+    const float* pmr = ws.pmax + ((int64_t)u * G + hg) * L.Umax;
     float* outb = out + (int64_t)bh * D;
 
-    // one round trip: the head's max, the union size and the first score tile
-    const uint32_t key = __ldcg(ws.head_max + bh);
+    // 1. the union size and the head's per-page maxima
     const int ucnt = __ldcg(ws.union_count + u);
-    float v[kTpvVec * 4];
+    float pm[kTpvPmVec];
 #pragma unroll
-    for (int j = 0; j < kTpvVec; ++j) {
-        const int i = (j * kTpvThreads + tid) * 4;     // zn is a multiple of 4
-        const float4 f = i < zn ? __ldcg(reinterpret_cast<const float4*>(z + i))
-                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+    for (int j = 0; j < kTpvPmVec; ++j) {
+        const int i = j * kTpvThreads + tid;
+        pm[j] = i < L.Umax ? __ldcg(pmr + i) : -INFINITY;
     }
-    const int n = ucnt * P;
-    if (key == 0u || n == 0) {
+    float mxl = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kTpvPmVec; ++j) {
+        if (j * kTpvThreads + tid < ucnt) mxl = fmaxf(mxl, pm[j]);
+        else pm[j] = -INFINITY;
+    }
+    for (int i = kTpvPmVec * kTpvThreads + tid; i < ucnt; i += kTpvThreads)
+        mxl = fmaxf(mxl, __ldcg(pmr + i));
+    const float mx = block_max(mxl, fred);
+    if (!(mx > -INFINITY)) {                  // no selected token
         for (int i = tid; i < D; i += blockDim.x) outb[i] = 0.f;
         if (tid == 0) {
             ws.tau[bh] = INFINITY;
@@ -869,27 +936,31 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
         }
         return;
     }
-    const float mx = key_float(key);
+    const int npl = list_candidate_pages(pm, pmr, ucnt, mx, s_pl, ired);   // ends with a barrier
 
-    // candidates x = z' - max > -1, compacted in a fixed thread order
+    // 2. the candidate pages' scores and blocks (all loads in flight before any
+    // is used); candidates x = z' - max > -1 in a fixed thread order, pos =
+    // index into the candidate pages' tokens
+    const int ne = npl << pshift;
+    const int* ublk = ws.union_blk + (int64_t)u * L.Umax;
     int m = 0;
-    for (int t0 = 0; t0 < n; t0 += kTpvTile) {
-        if (t0 > 0) {
-#pragma unroll
-            for (int j = 0; j < kTpvVec; ++j) {
-                const int i = t0 + (j * kTpvThreads + tid) * 4;
-                const float4 f = i < n ? __ldcg(reinterpret_cast<const float4*>(z + i))
-                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
-            }
-        }
-        int c = 0;
+    for (int t0 = 0; t0 < ne; t0 += kTpvTile) {
+        float v[kTpvVec * 4];
 #pragma unroll
         for (int j = 0; j < kTpvVec * 4; ++j) {
-            const int i = t0 + ((j >> 2) * kTpvThreads + tid) * 4 + (j & 3);
-            v[j] = i < n ? v[j] - mx : -INFINITY;
-            c += v[j] > -1.f;
+            const int f = t0 + j * kTpvThreads + tid;
+            v[j] = f < ne ? __ldcg(z + ((int64_t)s_pl[f >> pshift] << pshift) + (f & (P - 1))) : -INFINITY;
         }
+        if (t0 == 0) {
+            const int blk0 = tid < npl ? __ldcg(ublk + s_pl[tid]) : -1;
+            for (int k = tid + kTpvThreads; k < npl; k += kTpvThreads) s_pb[k] = __ldcg(ublk + s_pl[k]);
+            if (tid < npl) s_pb[tid] = blk0;
+        }
+#pragma unroll
+        for (int j = 0; j < kTpvVec * 4; ++j) v[j] -= mx;
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < kTpvVec * 4; ++j) c += v[j] > -1.f;
         int tot;
         int pos = m + block_exclusive_scan(c, ired, &tot);
 #pragma unroll
@@ -897,17 +968,17 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
             if (v[j] > -1.f) {
                 if (pos < cand_cap) {
                     s_x[pos] = v[j];
-                    s_pos[pos] = t0 + ((j >> 2) * kTpvThreads + tid) * 4 + (j & 3);
+                    s_pos[pos] = t0 + j * kTpvThreads + tid;
                 }
                 ++pos;
             }
         }
         m += tot;
     }
-    m = min(m, cand_cap);
+    m = min(m, cand_cap);                     // the candidates are selected tokens: m <= cand_cap
     __syncthreads();
 
-    // threshold t (relative to the max): f(t) = sum (x - t)_+^e - 1 = 0
+    // 3. threshold t (relative to the max): f(t) = sum (x - t)_+^e - 1 = 0
     float t;
     if (E != 0 && m <= 1024) {
         // one warp, candidates in registers, shuffle-only reductions
@@ -958,11 +1029,12 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
         t = 0.5f * (lo + hi);
     }
 
-    // weights, the support compacted per warp, then its V rows
+    // 4. weights, the support compacted per warp (V rows resolved from the
+    // candidate pages' blocks), then the support's V rows
     const float ex = 1.f / (alpha - 1.f);
     float wsum = 0.f;
-    const int cnt = weigh_support<E>(s_x, s_pos, m, t, ex, ws.vtok + (int64_t)u * L.nvw, wsum);
-    resolve_support_rows(s_pos, m, cnt, ws.union_blk + (int64_t)u * L.Umax, P, Hkv, kvh);
+    const int cnt = weigh_listed_support<E>(s_x, s_pos, m, t, ex, s_pl, s_pb, pshift, Hkv, kvh,
+                                            ws.vtok + (int64_t)u * L.nvw, wsum);
     if (lane == 0) s_wcnt[wid] = cnt;
     wsum = block_sum(wsum, fred);      // includes a barrier: weights, rows and counts are visible
     int sup = 0;
@@ -1035,12 +1107,12 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
 
     const uint32_t key = __ldcg(ws.head_max + bh);
     const int ucnt = __ldcg(ws.union_count + u);
-    const float* pmr = ws.pmax + (int64_t)u * L.Umax * G + hg;     // stride G
+    const float* pmr = ws.pmax + ((int64_t)u * G + hg) * L.Umax;     // head-major
     float pm[kTpvPmVec];
 #pragma unroll
     for (int j = 0; j < kTpvPmVec; ++j) {
         const int i = j * kTpvgThreads + tid;
-        pm[j] = i < L.Umax ? __ldcg(pmr + (int64_t)i * G) : -INFINITY;
+        pm[j] = i < L.Umax ? __ldcg(pmr + i) : -INFINITY;
     }
     const int n = ucnt * P;
     if (key == 0u || n == 0) {
@@ -1057,7 +1129,7 @@ tpv_global_kernel(int Hq, float alpha, KV kv, WS ws, DecodeLayout L, float* __re
     // pages that can hold a candidate, then their candidates x = z' - max >
     // -1, compacted in a fixed thread order
     int* pl = ws.plist + (int64_t)bh * L.Umax;
-    const int npl = list_candidate_pages(pm, pmr, G, ucnt, mx, pl, ired);   // ends with a barrier
+    const int npl = list_candidate_pages(pm, pmr, ucnt, mx, pl, ired);   // ends with a barrier
     int m = 0;
     const int ne = npl * P;
     for (int t0 = 0; t0 < ne; t0 += kTpvgTile) {
@@ -1350,7 +1422,7 @@ pv_softmax_kernel(int Hq, KV kv, WS ws, DecodeLayout L, int ns) {
         __syncwarp();        // every lane is done with stage st and s_w before they are refilled
     }
     if (failed) {
-        if (lane == 0) flag_bad_data();
+        if (lane == 0) flag_timeout();
         return;
     }
     if (cur_u >= 0) flush();
@@ -1522,7 +1594,7 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
     const int cand_cap = cap * kv.P;
     cudaError_t e;
     if (cand_cap > kTpvSmemCand) {
-        if (!ws.cand_x || !ws.plist || L.ccap < cand_cap) return cudaErrorInvalidValue;
+        if (!ws.cand_x || !ws.plist || L.ccap < cand_cap) return kShapeUnsupported;
         stage_mark(2, s);
         e = launch_kernel(tpv_global_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvgThreads), 0, s, Hq,
                           alpha, kv, ws, L, out, tau_out, support_out);
@@ -1530,7 +1602,7 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
         stage_mark(3, s);
         return cudaSuccess;
     }
-    const size_t smem = (size_t)cand_cap * 8 + (size_t)RG * D * sizeof(float);
+    const size_t smem = (size_t)cand_cap * 8 + (size_t)RG * D * sizeof(float) + (size_t)L.Umax * 8;
     e = cudaFuncSetAttribute(tpv_kernel<T, D, E>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1552,7 +1624,7 @@ static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv,
         const int page_bytes = kv.P * D * 2;
         const int ns = std::min(8, kQmStageBytes / page_bytes);
         const size_t smem = (size_t)kQmWarps * ns * page_bytes + (size_t)(L.U + 1) * sizeof(int);
-        if (ns < 2) return cudaErrorInvalidValue;
+        if (ns < 2) return kShapeUnsupported;
         auto kernel = pm ? qk_mma_kernel<D, G, true> : qk_mma_kernel<D, G, false>;
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -1566,7 +1638,7 @@ static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv,
         const size_t per_slot = page_bytes + sizeof(QkInfo) + 16;
         int ns = (int)std::min<size_t>(kQkMaxSlots, (kQkSmemBudget - fixed) / per_slot);
         ns = (ns / kQkConsumers) * kQkConsumers;
-        if (ns < kQkConsumers) return cudaErrorInvalidValue;
+        if (ns < kQkConsumers) return kShapeUnsupported;
         const size_t smem = fixed + (size_t)ns * per_slot;
         e = cudaFuncSetAttribute(qk_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -1583,9 +1655,8 @@ template <typename T, int D, int G>
 static cudaError_t launch_qk_tpv(const float* q, int Hq, float scale, const KV& kv, int cap,
                                  float alpha, float* out, float* tau_out, int32_t* support_out,
                                  const WS& ws, const DecodeLayout& L, cudaStream_t s) {
-    // page maxima only where the threshold kernel scans large selections
-    cudaError_t e = launch_qk<T, D, G>(q, Hq, (alpha - 1.f) * scale, kv, ws, L,
-                                       cap * kv.P > kTpvSmemCand, s);
+    // both threshold kernels start from each head's per-page maxima
+    cudaError_t e = launch_qk<T, D, G>(q, Hq, (alpha - 1.f) * scale, kv, ws, L, true, s);
     if (e != cudaSuccess) return e;
     const int E = fabsf(alpha - 1.5f) < 1e-6f ? 2 : (fabsf(alpha - 2.f) < 1e-6f ? 1 : 0);
     if (E == 2) return launch_tpv<2, T, D>(alpha, Hq, kv, ws, L, cap, out, tau_out, support_out, s);
@@ -1597,16 +1668,19 @@ template <typename T, int D, int G>
 static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV& kv,
                                    const int32_t* sel, const int32_t* n_sel, int cap, float alpha,
                                    float* out, float* tau_out, int32_t* support_out, const WS& ws,
-                                   const DecodeLayout& L, cudaStream_t s) {
+                                   const DecodeLayout& L, cudaStream_t s, bool planned) {
     cudaError_t e;
-    if (L.U > kMaxUnits || cap > kPlanSelRegs * kPlanThreads / G) return cudaErrorInvalidValue;
+    if (L.U > kMaxUnits || cap > kPlanSelRegs * kPlanThreads / G) return kShapeUnsupported;
     stage_mark(0, s);
-    const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax);
-    e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = launch_kernel(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel, cap,
-                      ws, L);
-    if (e != cudaSuccess) return e;
+    if (!planned) {
+        const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax, cap);
+        e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        e = launch_kernel(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel,
+                          n_sel, cap, ws, L);
+        if (e != cudaSuccess) return e;
+    }
     return launch_qk_tpv<T, D, G>(q, Hq, scale, kv, cap, alpha, out, tau_out, support_out, ws, L, s);
 }
 
@@ -1615,7 +1689,7 @@ static cudaError_t launch_decode_full_t(const float* q, int Hq, float scale, con
                                         float alpha, float* out, float* tau_out,
                                         int32_t* support_out, const WS& ws, const DecodeLayout& L,
                                         cudaStream_t s) {
-    if (L.U > kMaxUnits || L.Umax != kv.maxp) return cudaErrorInvalidValue;
+    if (L.U > kMaxUnits || L.Umax != kv.maxp) return kShapeUnsupported;
     stage_mark(0, s);
     const int chunks = (kv.maxp + kPlanAllChunk - 1) / kPlanAllChunk;
     cudaError_t e = launch_kernel(plan_all_kernel, dim3(L.U, chunks), dim3(kPlanThreads), 0, s, kv, Hq,
@@ -1628,14 +1702,14 @@ static cudaError_t launch_decode_full_t(const float* q, int Hq, float scale, con
 cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, const int32_t* sel,
                           const int32_t* n_sel, int cap, float alpha, float* out, float* tau_out,
                           int32_t* support_out, void* ws_base, const DecodeLayout& L,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool planned) {
     const WS ws = ws_views(ws_base, L);
     const int G = L.G;
     EKV_DISPATCH_T(kv.dtype, EKV_DISPATCH_D(kv.D, EKV_DISPATCH_G(G, {
         return launch_decode_t<T, kD, kG>(q, Hq, scale, kv, sel, n_sel, cap, alpha, out, tau_out,
-                                           support_out, ws, L, s);
+                                           support_out, ws, L, s, planned);
     })))
-    return cudaErrorInvalidValue;
+    return kShapeUnsupported;
 }
 
 template <typename T, int D, int G>
@@ -1644,15 +1718,15 @@ static cudaError_t launch_decode_softmax_t(const float* q, int Hq, float scale, 
                                            bool full, float* out, float* lse_out, const WS& ws,
                                            const DecodeLayout& L, cudaStream_t s) {
     cudaError_t e;
-    if (L.U > kMaxUnits || !ws.recs) return cudaErrorInvalidValue;
+    if (L.U > kMaxUnits || !ws.recs) return kShapeUnsupported;
     stage_mark(0, s);
     if (full) {
-        if (L.Umax != kv.maxp) return cudaErrorInvalidValue;
+        if (L.Umax != kv.maxp) return kShapeUnsupported;
         const int chunks = (kv.maxp + kPlanAllChunk - 1) / kPlanAllChunk;
         e = launch_kernel(plan_all_kernel, dim3(L.U, chunks), dim3(kPlanThreads), 0, s, kv, Hq, ws, L);
     } else {
-        if (cap > kPlanSelRegs * kPlanThreads / G) return cudaErrorInvalidValue;
-        const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax);
+        if (cap > kPlanSelRegs * kPlanThreads / G) return kShapeUnsupported;
+        const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax, cap);
         e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         e = launch_kernel(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel,
@@ -1689,7 +1763,7 @@ cudaError_t launch_decode_softmax(const float* q, int Hq, float scale, const KV&
         return launch_decode_softmax_t<T, kD, kG>(q, Hq, scale, kv, sel, n_sel, cap, full, out,
                                                    lse_out, ws, L, s);
     })))
-    return cudaErrorInvalidValue;
+    return kShapeUnsupported;
 }
 
 cudaError_t launch_decode_full(const float* q, int Hq, float scale, const KV& kv, float alpha,
@@ -1701,7 +1775,7 @@ cudaError_t launch_decode_full(const float* q, int Hq, float scale, const KV& kv
         return launch_decode_full_t<T, kD, kG>(q, Hq, scale, kv, alpha, out, tau_out, support_out,
                                                 ws, L, s);
     })))
-    return cudaErrorInvalidValue;
+    return kShapeUnsupported;
 }
 
 }  // namespace ekv

@@ -36,7 +36,7 @@ struct KV {
 // The softmax decode adds partial-sum records (recs, nrec slots of G * (D + 1)
 // floats): one slot per streaming warp plus one per unit.
 //
-// pmax [U][Umax][G] holds each head's largest z' on each union page (-inf
+// pmax [U][G][Umax] holds each head's largest z' on each union page (-inf
 // where the head did not select it); plist [B * Hq][Umax] is the global page
 // list of the large-selection threshold kernel (with cand_x / cand_pos).
 struct DecodeLayout {
@@ -56,14 +56,22 @@ cudaError_t launch_build_meta(const KV& kv, int first_page, int num_pages, void*
 cudaError_t launch_score(const float* q, int Hq, float scale, const KV& kv, const void* kmin,
                          const void* kmax, const float* mean, const float* var, int policy,
                          float* out, cudaStream_t s);
+// Top-k selection.  With plan_ws / plan_layout (a decode workspace and its
+// layout) the selection may also write the decode's union plan into it; then
+// *planned is set and the decode can skip its plan (launch_decode planned).
 cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp, int32_t* sel,
-                               int32_t* n_sel, float* aux, bool shared, cudaStream_t s);
+                               int32_t* n_sel, float* aux, bool shared, cudaStream_t s,
+                               void* plan_ws = nullptr, const DecodeLayout* plan_layout = nullptr,
+                               bool* planned = nullptr);
 cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, float alpha,
                                 float delta, int32_t* sel, int32_t* n_sel, float* aux,
                                 cudaStream_t s);
+// planned: the union plan of this selection is already in the workspace (it
+// was written by launch_select_topk), so the plan kernel is skipped.
 cudaError_t launch_decode(const float* q, int Hq, float scale, const KV& kv, const int32_t* sel,
                           const int32_t* n_sel, int cap, float alpha, float* out, float* tau_out,
-                          int32_t* support_out, void* ws, const DecodeLayout& L, cudaStream_t s);
+                          int32_t* support_out, void* ws, const DecodeLayout& L, cudaStream_t s,
+                          bool planned = false);
 // Softmax attention over the selected pages (full: every page), laid out by
 // softmax_layout; lse_out (nullable) receives log sum_i e^(z_i).
 cudaError_t launch_decode_softmax(const float* q, int Hq, float scale, const KV& kv,
@@ -92,12 +100,21 @@ void set_decode_stage_events(const cudaEvent_t* events, int n);
 cudaError_t read_decode_counts(void* ws, const DecodeLayout& L, int32_t* union_pages,
                                int32_t* v_rows, cudaStream_t s);
 
-// Sticky device-data check words, one per translation unit: read, OR'd into
-// *flag, and cleared.
+// Returned by the launchers for a shape or size outside what the kernels
+// support (reported as EKV_UNSUPPORTED); every other error is a CUDA failure.
+constexpr cudaError_t kShapeUnsupported = cudaErrorNotSupported;
+
+// Sticky device status words, one per translation unit: read, OR'd into
+// *flag (bit 0 malformed data, bit 1 a bounded wait gave up), and cleared.
 cudaError_t take_status_meta(int* flag, cudaStream_t s);
 cudaError_t take_status_score(int* flag, cudaStream_t s);
 cudaError_t take_status_select(int* flag, cudaStream_t s);
 cudaError_t take_status_decode(int* flag, cudaStream_t s);
+cudaError_t take_status_selfcheck(int* flag, cudaStream_t s);
+
+// One kernel whose bounded wait on an mbarrier that never completes gives up
+// after limit_ns and records the timeout bit (self-check of the give-up path).
+cudaError_t launch_wait_timeout_check(uint64_t limit_ns, cudaStream_t s);
 
 // Limits of the selection kernels (pages held in shared memory per head).
 constexpr int kMaxPagesTopk = 49152;
@@ -105,11 +122,13 @@ constexpr int kMaxPagesGauss = 12288;
 
 }  // namespace ekv
 
-// Per-TU definition of the status word and its host accessor.
+// Per-TU definition of the status word and its host accessor.  Bit 0: the
+// kernels met malformed device data (skipped); bit 1: a bounded wait gave up.
 #define EKV_DEFINE_STATUS(NAME)                                                        \
     namespace ekv {                                                                    \
     static __device__ int g_status_word;                                               \
     __device__ __forceinline__ void flag_bad_data() { atomicOr(&g_status_word, 1); }  \
+    __device__ __forceinline__ void flag_timeout() { atomicOr(&g_status_word, 2); }   \
     cudaError_t take_status_##NAME(int* flag, cudaStream_t s) {                        \
         int v = 0;                                                                     \
         cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_status_word, sizeof(int), 0,   \
@@ -121,7 +140,7 @@ constexpr int kMaxPagesGauss = 12288;
             e = cudaMemcpyToSymbolAsync(g_status_word, &zero, sizeof(int), 0,          \
                                         cudaMemcpyHostToDevice, s);                    \
             if (e == cudaSuccess) e = cudaStreamSynchronize(s);                        \
-            *flag |= 1;                                                                \
+            *flag |= v;                                                                \
         }                                                                              \
         return e;                                                                      \
     }                                                                                  \
@@ -132,7 +151,7 @@ constexpr int kMaxPagesGauss = 12288;
     switch (D_) {                                        \
         case 64: { constexpr int kD = 64; __VA_ARGS__; } break;   \
         case 128: { constexpr int kD = 128; __VA_ARGS__; } break; \
-        default: return cudaErrorInvalidValue;           \
+        default: return ::ekv::kShapeUnsupported;        \
     }
 #define EKV_DISPATCH_G(G_, ...)                          \
     switch (G_) {                                        \
@@ -140,7 +159,7 @@ constexpr int kMaxPagesGauss = 12288;
         case 2: { constexpr int kG = 2; __VA_ARGS__; } break; \
         case 4: { constexpr int kG = 4; __VA_ARGS__; } break; \
         case 8: { constexpr int kG = 8; __VA_ARGS__; } break; \
-        default: return cudaErrorInvalidValue;           \
+        default: return ::ekv::kShapeUnsupported;        \
     }
 #define EKV_DISPATCH_T(DT_, ...)                         \
     if ((DT_) == 1) { using T = ::ekv::bf16raw; __VA_ARGS__; } \

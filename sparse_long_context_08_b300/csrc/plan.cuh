@@ -20,7 +20,7 @@ struct WS {
     uint32_t* vtok;       // [U][nvw] tokens whose V row was read
     int* vrows;           // per-unit popcount of vtok (measurement)
     float* z;             // [U][G][Umax * P]
-    float* pmax;          // [U][Umax][G] largest z' of each union page per head
+    float* pmax;          // [U][G][Umax] largest z' of each union page per head
     float* tau;
     float* cand_x;        // [B * Hq][ccap] candidates, then weights (large selections only)
     int* cand_pos;        // [B * Hq][ccap] their score index, then V row
@@ -44,60 +44,38 @@ __device__ __forceinline__ int pages_of(const KV& kv, int b) {
     return min(kv.maxp, (kv.sl[b] + kv.P - 1) / kv.P);
 }
 
-// Shared memory build_plan needs: [G][ceil(max_pages/32)] bitmap words plus
-// [Umax] union pages (ints).
-inline size_t plan_smem_bytes(int G, int max_pages, int Umax) {
-    return (size_t)G * ((max_pages + 31) / 32) * 4 + (size_t)Umax * 4;
+// Shared memory build_plan needs: [G][ceil(max_pages/32)] bitmap words,
+// [Umax] union pages and [G * cap] staged selection entries (ints).
+inline size_t plan_smem_bytes(int G, int max_pages, int Umax, int cap) {
+    return (size_t)G * ((max_pages + 31) / 32) * 4 + (size_t)Umax * 4 + (size_t)G * cap * 4;
 }
 
-// Union plan of unit u = (sequence b, kv head): the ascending union of the G
-// heads' selected pages, each page's head mask and physical block; also resets
-// the unit's per-call state (head maxima, V-row marks).  Called by every
-// thread of the block; needs G * cap <= kPlanSelRegs * blockDim.x.  `s_bits`
-// and `s_upage` as sized by plan_smem_bytes, `red` >= 40 ints, `s_ns` >= G.
+// The union plan of unit u from its G heads' selection rows already in
+// shared memory (s_sel [G][cap], s_ns [G] counts, each in [0, cap]): the
+// ascending union of the pages, each page's head mask and physical block, and
+// the union size.  Called by every thread of the block; s_bits ([G][nwm]
+// words) and s_upage ([Umax]) are scratch; `red` >= 40 ints.  Pages outside
+// the sequence are skipped and flagged.
 template <int G>
-__device__ void build_plan(const KV& kv, int Hq, const int32_t* __restrict__ sel,
-                           const int32_t* __restrict__ n_sel, int cap, const WS& ws,
-                           const DecodeLayout& L, int u, uint32_t* s_bits, int* s_upage,
-                           int* red, int* s_ns) {
+__device__ void plan_from_rows(const KV& kv, int cap, const WS& ws, const DecodeLayout& L, int u,
+                               const int* s_sel, const int* s_ns, uint32_t* s_bits, int* s_upage,
+                               int* red) {
     const int nwm = (kv.maxp + 31) / 32;
     const int b = u / kv.hkv;
-    const int kvh = u - b * kv.hkv;
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int bh0 = b * Hq + kvh * G;
-    // one round trip: the counts and, speculatively, every selection row in
-    // full (entries past a head's count are read but not used)
-    if (tid < G) s_ns[tid] = __ldcg(n_sel + bh0 + tid);
-    int pv[kPlanSelRegs];
-#pragma unroll
-    for (int k = 0; k < kPlanSelRegs; ++k) {
-        const int e = tid + k * nt;
-        pv[k] = e < G * cap ? __ldcg(sel + (int64_t)bh0 * cap + e) : -1;
-    }
     const int np = pages_of(kv, b);
     const int nw = (np + 31) / 32;
     for (int i = tid; i < G * nw; i += nt) {
         const int h = i / nw;
         s_bits[h * nwm + (i - h * nw)] = 0u;
     }
-    if (tid < G) ws.head_max[bh0 + tid] = 0u;
-    for (int i = tid; i < L.nvw; i += nt) ws.vtok[(int64_t)u * L.nvw + i] = 0u;
     __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kPlanSelRegs; ++k) {
-        const int e = tid + k * nt;
-        if (e < G * cap) {
-            const int h = e / cap, r = e - h * cap;
-            int ns = s_ns[h];
-            if (ns < 0 || ns > cap) {
-                if (r == 0) flag_bad_data();
-                ns = max(0, min(ns, cap));
-            }
-            if (r < ns) {
-                const int p = pv[k];
-                if (p >= 0 && p < np) atomicOr(&s_bits[h * nwm + (p >> 5)], 1u << (p & 31));
-                else flag_bad_data();
-            }
+    for (int e = tid; e < G * cap; e += nt) {
+        const int h = e / cap, r = e - h * cap;
+        if (r < s_ns[h]) {
+            const int p = s_sel[e];
+            if (p >= 0 && p < np) atomicOr(&s_bits[h * nwm + (p >> 5)], 1u << (p & 31));
+            else flag_bad_data();
         }
     }
     __syncthreads();
@@ -144,6 +122,57 @@ __device__ void build_plan(const KV& kv, int Hq, const int32_t* __restrict__ sel
         ublk[i] = blk;
     }
     if (tid == 0) ws.union_count[u] = total;
+}
+
+// Resets unit u's per-call state: its heads' maxima and V-row marks.
+__device__ __forceinline__ void plan_reset_unit(int Hq, int G, const WS& ws, const DecodeLayout& L,
+                                                const KV& kv, int u) {
+    const int b = u / kv.hkv, kvh = u - b * kv.hkv;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    if (tid < G) ws.head_max[b * Hq + kvh * G + tid] = 0u;
+    for (int i = tid; i < L.nvw; i += nt) ws.vtok[(int64_t)u * L.nvw + i] = 0u;
+}
+
+// Union plan of unit u = (sequence b, kv head) from the selection in global
+// memory: the counts and every row entry are staged in shared memory in one
+// round trip (entries past a head's count are read but not used), then
+// plan_from_rows; also resets the unit's per-call state.  Needs G * cap <=
+// kPlanSelRegs * blockDim.x; `s_bits`, `s_upage` and `s_sel` as sized by
+// plan_smem_bytes, `red` >= 40 ints, `s_ns` >= G.
+template <int G>
+__device__ void build_plan(const KV& kv, int Hq, const int32_t* __restrict__ sel,
+                           const int32_t* __restrict__ n_sel, int cap, const WS& ws,
+                           const DecodeLayout& L, int u, uint32_t* s_bits, int* s_upage,
+                           int* s_sel, int* red, int* s_ns) {
+    const int b = u / kv.hkv;
+    const int kvh = u - b * kv.hkv;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int bh0 = b * Hq + kvh * G;
+    const int ns_reg = tid < G ? __ldcg(n_sel + bh0 + tid) : 0;
+    int pv[kPlanSelRegs];
+#pragma unroll
+    for (int k = 0; k < kPlanSelRegs; ++k) {
+        const int e = tid + k * nt;
+        pv[k] = e < G * cap ? __ldcg(sel + (int64_t)bh0 * cap + e) : -1;
+    }
+    plan_reset_unit(Hq, G, ws, L, kv, u);
+    // the entries go to shared memory before the barrier: their loads complete
+    // here, in one round trip with the counts
+#pragma unroll
+    for (int k = 0; k < kPlanSelRegs; ++k) {
+        const int e = tid + k * nt;
+        if (e < G * cap) s_sel[e] = pv[k];
+    }
+    if (tid < G) {
+        int ns = ns_reg;
+        if (ns < 0 || ns > cap) {
+            flag_bad_data();
+            ns = max(0, min(ns, cap));
+        }
+        s_ns[tid] = ns;
+    }
+    __syncthreads();
+    plan_from_rows<G>(kv, cap, ws, L, u, s_sel, s_ns, s_bits, s_upage, red);
 }
 
 }  // namespace ekv

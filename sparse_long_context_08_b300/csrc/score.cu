@@ -512,7 +512,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
             }
             if (u > 0 && !mbar_wait(&sh.empty[s], (u - 1) & 1)) {
                 *abort = 1;
-                if (lane == 0) flag_bad_data();
+                if (lane == 0) flag_timeout();
                 break;
             }
             unsigned char* st = ring + (size_t)s * C::A_BYTES;
@@ -533,7 +533,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
                 // the MMAs of every earlier stage (issued in order) must be done
                 if (j > 0 && !mbar_wait(&sh.empty[(j - 1) % S], ((j - 1) / S) & 1)) {
                     *abort = 1;
-                    if (lane == 0) flag_bad_data();
+                    if (lane == 0) flag_timeout();
                     break;
                 }
                 tc_build_b<D, G, HKV, kTcProd>(bbuf, q, scale, b_cur, tid);
@@ -549,13 +549,13 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
             constexpr uint32_t idesc = umma_idesc_bf16_f32<kTcRows, C::N>();
             const uint32_t sbb = smem_u32(bbuf);
             int issued = 0;
-            if (nt > 0 && !mbar_wait(&sh.binit, 0)) { *abort = 1; flag_bad_data(); }
+            if (nt > 0 && !mbar_wait(&sh.binit, 0)) { *abort = 1; flag_timeout(); }
             for (int j = 0; j < 2 * nt && !*abort; ++j) {
                 const int i = j >> 1, half = j & 1, s = j % S, u = j / S, a = i & 1, v = i >> 1;
                 if (!mbar_wait(&sh.full[s], u & 1) || !mbar_wait(&sh.bfull[s], u & 1) ||
                     (half == 0 && v > 0 && !mbar_wait(&sh.acce[a], (v - 1) & 1))) {
                     *abort = 1;
-                    flag_bad_data();
+                    flag_timeout();
                     break;
                 }
                 // the copies landed through the generic proxy: order them before
@@ -600,7 +600,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
             const int a = i & 1, v = i >> 1;
             if (!mbar_wait(&sh.accf[a], v & 1)) {
                 *abort = 1;
-                if (lane == 0) flag_bad_data();
+                if (lane == 0) flag_timeout();
                 break;
             }
             tc_fence_after();
@@ -675,14 +675,14 @@ static int sm_count_score() {
 template <typename T, int D, int G, bool kGauss>
 static cudaError_t launch_score_t(const float* q, int Hq, float scale, const KV& kv,
                                   const void* ma, const void* mb, float* out, cudaStream_t s) {
-    if (kv.B > kScoreMaxSeqs || kv.maxp >= (1 << 17)) return cudaErrorInvalidValue;
+    if (kv.B > kScoreMaxSeqs || kv.maxp >= (1 << 17)) return kShapeUnsupported;
     const int grid = sm_count_score() * kScoreCtasPerSm;
     const int64_t total_max = (int64_t)kv.B * kv.maxp;
     const int nloc_max = (int)((total_max + grid - 1) / grid) + 1;
     using C = ScoreCfg<T, D, G, kGauss>;
     const size_t ring_bytes = (size_t)kScoreWarps * kScoreStages * 2 * 32 * C::DPL * sizeof(T);
     const size_t smem = ring_bytes + (size_t)(kv.B + 1 + 2 * nloc_max) * sizeof(int);
-    if (smem > 110 * 1024) return cudaErrorInvalidValue;
+    if (smem > 110 * 1024) return kShapeUnsupported;
     cudaError_t e = cudaFuncSetAttribute(score_kernel<T, D, G, kGauss>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -718,7 +718,7 @@ cudaError_t launch_score(const float* q, int Hq, float scale, const KV& kv, cons
             return launch_score_t<T, kD, kG, false>(q, Hq, scale, kv, kmin, kmax, out, s);
         })))
     }
-    return cudaErrorInvalidValue;
+    return kShapeUnsupported;
 }
 
 }  // namespace ekv

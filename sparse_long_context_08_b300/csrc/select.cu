@@ -12,10 +12,14 @@
 // (F >= 0 there; F is convex and decreasing, so Newton climbs monotonically),
 // keeps pages whose (alpha-1) * estimated max clears tau-hat - delta, and caps
 // the kept set by estimated-max rank with the same radix select.
+#include <algorithm>
+
 #include "common.cuh"
 #include "mills_ratio.h"
 
 EKV_DEFINE_STATUS(select)
+
+#include "plan.cuh"
 
 namespace ekv {
 
@@ -313,6 +317,377 @@ select_topk_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Top-k by bound with register-resident keys (the default path).
+//
+// A CTA of kTkThreads threads holds up to kTkThreads * KPT keys, thread t the
+// consecutive pages [t KPT, (t + 1) KPT) of its range, so the ascending page
+// order of the output is the thread order.  The k-th largest key is found by
+// an MSB radix select with 11-bit digits that starts at the highest bit where
+// the range's keys differ and stops as soon as the boundary bin is taken whole
+// (typically two passes over 4096 keys); ties at the k-th key go to the lower
+// pages.  One packed block scan of (above, boundary-bin) counts places every
+// taken page.
+//
+// Long sequences split their pages over a thread-block cluster of C <= 8
+// CTAs: each CTA takes the top min(k, its pages) of its contiguous range and
+// writes them, in page order, with their keys into the rank-0 CTA's shared
+// memory (distributed shared memory); after one cluster barrier the rank-0
+// CTA selects the k best of those candidates.  Every page of the global top k
+// is in its range's top k (the order (bound desc, page asc) is total), so the
+// result is the single-CTA one.
+// ---------------------------------------------------------------------------
+constexpr int kTkThreads = 512;
+constexpr int kTkDigitBits = 11;
+constexpr int kTkBins = 1 << kTkDigitBits;
+constexpr int kTkMaxCluster = 8;
+
+struct TkShared {
+    int hist[kTkBins];
+    int red[40];
+    uint32_t umin[32], umax[32];
+    int digit, above, nb;
+    int cnt[kTkMaxCluster];          // rank-0 CTA: candidates each rank wrote
+    uint32_t next[kTkMaxCluster];    // and the largest key each rank left out
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+// Split cluster barrier: arrive now, wait later (every CTA of the cluster has
+// started once the wait returns, so its shared memory can be written).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+// 32-bit store into the shared memory of CTA `rank` of this cluster, at the
+// address `p` has in this CTA.
+__device__ __forceinline__ void st_cluster_u32(const void* p, uint32_t rank, uint32_t v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+
+// Block-wide min and max of one value per thread (every thread gets both).
+__device__ __forceinline__ void tk_minmax(uint32_t& mn, uint32_t& mx, TkShared& sh) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    __syncthreads();
+    if (lane == 0) { sh.umin[wid] = mn; sh.umax[wid] = mx; }
+    __syncthreads();
+    mn = lane < nw ? sh.umin[lane] : 0xFFFFFFFFu;
+    mx = lane < nw ? sh.umax[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+}
+
+// The boundary of the k largest among this block's valid keys (bit j of
+// `valid` marks key[j]; 1 <= k <= the number of valid keys; kmn/kmx their
+// extremes).  Key x is taken iff (x >> shift) > hi, or (x >> shift) == hi and
+// fewer than takeB such keys precede it in key order.  sh.hist must be zero on
+// entry and is zero again on return.
+template <int KPT>
+__device__ void tk_boundary(const uint32_t (&key)[KPT], uint32_t valid, int n, int k,
+                            uint32_t kmn, uint32_t kmx, TkShared& sh, int& shift_out,
+                            uint64_t& hi_out, int& takeB_out) {
+    constexpr int BPT = kTkBins / kTkThreads;          // bins per thread
+    const int tid = threadIdx.x;
+    const uint32_t diff = kmn ^ kmx;
+    int shift = diff ? 32 - __clz(diff) : 0;
+    uint64_t hi = (uint64_t)kmx >> shift;
+    int rem = k, nB = n;
+    while (shift > 0 && nB != rem) {
+        const int dbits = min(kTkDigitBits, shift);
+        shift -= dbits;
+        const uint32_t dmask = (1u << dbits) - 1u;
+#pragma unroll
+        for (int j = 0; j < KPT; ++j)
+            if (((valid >> j) & 1u) && ((uint64_t)key[j] >> (shift + dbits)) == hi)
+                atomicAdd(&sh.hist[(key[j] >> shift) & dmask], 1);
+        __syncthreads();
+        int c[BPT], local = 0;
+#pragma unroll
+        for (int b = 0; b < BPT; ++b) { c[b] = sh.hist[tid * BPT + b]; local += c[b]; }
+        int total;
+        const int pre = block_exclusive_scan(local, sh.red, &total);
+        int acc = total - pre - local;                  // keys in the bins above this thread's
+#pragma unroll
+        for (int b = BPT - 1; b >= 0; --b) {
+            if (acc < rem && acc + c[b] >= rem) { sh.digit = tid * BPT + b; sh.above = acc; sh.nb = c[b]; }
+            acc += c[b];
+        }
+        __syncthreads();
+        const int d = sh.digit;
+        rem -= sh.above;
+        nB = sh.nb;
+        hi = (hi << dbits) | (uint64_t)d;
+#pragma unroll
+        for (int b = 0; b < BPT; ++b) sh.hist[tid * BPT + b] = 0;
+        __syncthreads();
+    }
+    shift_out = shift;
+    hi_out = hi;
+    takeB_out = rem;
+}
+
+// Output positions of this thread's taken keys (in key order) given the
+// boundary; calls f(j, pos) for each taken key j.  Also returns the smallest
+// taken and largest untaken valid key of the block (0 / 0 if none).
+template <int KPT, typename F>
+__device__ __forceinline__ void tk_place(const uint32_t (&key)[KPT], uint32_t valid, int shift,
+                                         uint64_t hi, int takeB, TkShared& sh, F&& f,
+                                         uint32_t& tmin, uint32_t& nmax) {
+    int a = 0, b = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+        if ((valid >> j) & 1u) {
+            const uint64_t kh = (uint64_t)key[j] >> shift;
+            a += kh > hi;
+            b += kh == hi;
+        }
+    int total;
+    const int pre = block_exclusive_scan(a | (b << 16), sh.red, &total);
+    int ra = pre & 0xFFFF, rb = pre >> 16;
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+        if ((valid >> j) & 1u) {
+            const uint64_t kh = (uint64_t)key[j] >> shift;
+            bool take = false;
+            if (kh > hi) {
+                f(j, ra + min(rb, takeB));
+                ++ra;
+                take = true;
+            } else if (kh == hi) {
+                if (rb < takeB) { f(j, ra + rb); take = true; }
+                ++rb;
+            }
+            if (take) mn = min(mn, key[j]); else mx = max(mx, key[j]);
+        }
+    tk_minmax(mn, mx, sh);
+    tmin = mn;
+    nmax = mx;
+}
+
+// gs = 0: one head per CTA (csize CTAs per head); gs > 0: one (sequence, kv
+// head) per CTA group, keys = the largest bound of the group's gs query heads,
+// result written to every head of the group.  Dynamic shared memory: [kp]
+// ints (the output row), then, for csize > 1, the rank-0 candidate arrays
+// [C][slot] keys and pages.
+//
+// PG > 0 (csize = 1, PG = the group size): the selection also builds the
+// decode's union plan of each kv head (plan_from_rows) in the decode
+// workspace `ws`.  Per-head selections run as a cluster of the group's PG
+// CTAs: each writes its row into the rank-0 CTA's shared memory, which builds
+// the plan; shared selections give every head the CTA's own row.  Dynamic
+// shared memory then also holds [PG][kp] rows, [PG][max_pages / 32] bitmap
+// words and [Umax] union pages.
+template <int KPT, int PG>
+__global__ void __launch_bounds__(kTkThreads, 2)
+select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
+                       int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
+                       float* __restrict__ aux, int gs, int csize, WS ws, DecodeLayout L) {
+    extern __shared__ __align__(16) int32_t s_row[];
+    __shared__ TkShared sh;
+    __shared__ int s_cnt[8];
+    const int tid = threadIdx.x;
+    const int ng = gs > 0 ? gs : 1;
+    const int unit = blockIdx.x / csize;
+    const uint32_t rank = csize > 1 ? cluster_rank() : 0u;
+    const int bh = gs > 0 ? (unit / kv.hkv) * Hq + (unit % kv.hkv) * gs : unit;
+    const int b = bh / Hq;
+    // the CTA's range is fixed by max_pages, so the bounds are loaded (in
+    // bounds of the row) while the sequence length is still in flight; keys
+    // past the sequence's pages are masked out below
+    const int chunk = ((kv.maxp + csize - 1) / csize + 3) & ~3;    // a multiple of 4 pages
+    const int p0 = (int)rank * chunk;
+    const int span = max(0, min(kv.maxp - p0, chunk));
+    const float* src = bound + (int64_t)bh * kv.maxp + p0;
+    float v[KPT];
+    {
+        const bool vec = (kv.maxp & 3) == 0;
+        for (int g = 0; g < ng; ++g) {
+            const float* rs = src + (int64_t)g * kv.maxp;
+#pragma unroll
+            for (int j = 0; j < KPT; j += 4) {
+                const int i = tid * KPT + j;
+                float4 f;
+                if (vec && i + 3 < span) {
+                    f = __ldcg(reinterpret_cast<const float4*>(rs + i));
+                } else {
+                    f.x = i < span ? __ldcg(rs + i) : -INFINITY;
+                    f.y = i + 1 < span ? __ldcg(rs + i + 1) : -INFINITY;
+                    f.z = i + 2 < span ? __ldcg(rs + i + 2) : -INFINITY;
+                    f.w = i + 3 < span ? __ldcg(rs + i + 3) : -INFINITY;
+                }
+                if (g == 0) {
+                    v[j] = f.x; v[j + 1] = f.y; v[j + 2] = f.z; v[j + 3] = f.w;
+                } else {       // shared: the group's largest bound
+                    v[j] = fmaxf(v[j], f.x); v[j + 1] = fmaxf(v[j + 1], f.y);
+                    v[j + 2] = fmaxf(v[j + 2], f.z); v[j + 3] = fmaxf(v[j + 3], f.w);
+                }
+            }
+        }
+    }
+    const int np = min(kv.maxp, (kv.sl[b] + kv.P - 1) / kv.P);
+    const int k = min(kp, np);
+    // plan mode: the unit, and this CTA's head within it (its cluster rank)
+    const int pu = gs > 0 ? unit : bh / (PG > 0 ? PG : 1);
+    const uint32_t prank = (PG > 1 && gs == 0) ? cluster_rank() : 0u;
+    if (k <= 0) {                       // the same for every CTA of the cluster
+        if (rank == 0 && tid < ng) {
+            n_sel[bh + tid] = 0;
+            if (aux) { aux[2 * (bh + tid)] = INFINITY; aux[2 * (bh + tid) + 1] = -INFINITY; }
+        }
+        if constexpr (PG > 0) {
+            if (prank == 0) {           // an empty plan
+                plan_reset_unit(Hq, PG, ws, L, kv, pu);
+                if (tid == 0) ws.union_count[pu] = 0;
+            }
+        }
+        return;
+    }
+    if (csize > 1 || (PG > 1 && gs == 0)) cluster_arrive_relaxed();   // waited for before the first remote store
+    const int n_loc = max(0, min(np - p0, chunk));
+    for (int i = tid; i < kTkBins; i += kTkThreads) sh.hist[i] = 0;
+
+    // this thread's keys: pages p0 + [tid KPT, (tid + 1) KPT)
+    uint32_t key[KPT];
+    uint32_t valid = 0u;
+    {
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+            key[j] = float_key(v[j]);
+            if (tid * KPT + j < n_loc) valid |= 1u << j;
+        }
+    }
+    uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+        if ((valid >> j) & 1u) { kmn = min(kmn, key[j]); kmx = max(kmx, key[j]); }
+    tk_minmax(kmn, kmx, sh);
+
+    const int k_loc = min(kp, n_loc);
+    int shift, takeB;
+    uint64_t hi;
+    uint32_t tmin, nmax;
+    if (csize == 1) {
+        tk_boundary<KPT>(key, valid, n_loc, k_loc, kmn, kmx, sh, shift, hi, takeB);
+        tk_place<KPT>(key, valid, shift, hi, takeB, sh,
+                      [&](int j, int pos) { s_row[pos] = tid * KPT + j; }, tmin, nmax);
+        // tk_place ends with a barrier: s_row is complete
+        for (int x = tid; x < ng * k; x += kTkThreads) {
+            const int g = x / k, r = x - g * k;
+            sel[(int64_t)(bh + g) * kp + r] = s_row[r];
+        }
+        if (tid < ng) {
+            n_sel[bh + tid] = k;
+            if (aux) {
+                aux[2 * (bh + tid)] = key_float(tmin);
+                aux[2 * (bh + tid) + 1] = k < np ? key_float(nmax) : -INFINITY;
+            }
+        }
+        if constexpr (PG > 0) {
+            const int nwm = (kv.maxp + 31) / 32;
+            int* c_rows = s_row + kp;                                      // [PG][kp]
+            uint32_t* s_bits = reinterpret_cast<uint32_t*>(c_rows + PG * kp);
+            int* s_upage = reinterpret_cast<int*>(s_bits + PG * nwm);
+            if (gs > 0 || PG == 1) {
+                // one row for every head of the group
+                for (int x = tid; x < PG * k; x += kTkThreads) {
+                    const int g = x / k, r = x - g * k;
+                    c_rows[g * kp + r] = s_row[r];
+                }
+                if (tid < PG) s_cnt[tid] = k;
+            } else {
+                cluster_wait();         // every CTA of the cluster is running
+                for (int r = tid; r < k; r += kTkThreads)
+                    st_cluster_u32(c_rows + prank * kp + r, 0u, static_cast<uint32_t>(s_row[r]));
+                if (tid == 0) st_cluster_u32(&s_cnt[prank], 0u, static_cast<uint32_t>(k));
+                cluster_sync_all();     // the rows are in the rank-0 CTA
+                if (prank != 0) return; // nothing reads another CTA's memory past here
+            }
+            plan_reset_unit(Hq, PG, ws, L, kv, pu);
+            __syncthreads();
+            plan_from_rows<PG>(kv, kp, ws, L, pu, c_rows, s_cnt, s_bits, s_upage, sh.red);
+        }
+        return;
+    }
+
+    // cluster: this range's top k_loc, in page order, to the rank-0 CTA
+    const int slot = min(kp, chunk);
+    uint32_t* c_key = reinterpret_cast<uint32_t*>(s_row + kp);
+    int32_t* c_page = reinterpret_cast<int32_t*>(c_key + csize * slot);
+    cluster_wait();                     // every CTA of the cluster is running
+    if (n_loc > 0) {
+        tk_boundary<KPT>(key, valid, n_loc, k_loc, kmn, kmx, sh, shift, hi, takeB);
+        tk_place<KPT>(key, valid, shift, hi, takeB, sh,
+                      [&](int j, int pos) {
+                          st_cluster_u32(c_key + rank * slot + pos, 0u, key[j]);
+                          st_cluster_u32(c_page + rank * slot + pos, 0u,
+                                         static_cast<uint32_t>(p0 + tid * KPT + j));
+                      }, tmin, nmax);
+    } else {
+        nmax = 0u;
+    }
+    if (tid == 0) {
+        st_cluster_u32(&sh.cnt[rank], 0u, static_cast<uint32_t>(k_loc > 0 ? k_loc : 0));
+        st_cluster_u32(&sh.next[rank], 0u, k_loc < n_loc ? nmax : 0u);
+    }
+    cluster_sync_all();                 // candidates visible in the rank-0 CTA
+    if (rank != 0) return;              // nothing reads another CTA's memory past here
+
+    // rank 0: the k best of the candidates; flat position x = r * slot + i
+    // (i < cnt[r]) is ascending in page order
+    uint32_t ck[KPT];
+    uint32_t cvalid = 0u;
+    int m = 0;
+    uint32_t out_next = 0u;
+    for (int r = 0; r < csize; ++r) { m += sh.cnt[r]; out_next = max(out_next, sh.next[r]); }
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int x = tid * KPT + j;
+        const int r = x / slot, i = x - r * slot;
+        ck[j] = 0u;
+        if (r < csize && i < sh.cnt[r]) { ck[j] = c_key[x]; cvalid |= 1u << j; }
+    }
+    kmn = 0xFFFFFFFFu;
+    kmx = 0u;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+        if ((cvalid >> j) & 1u) { kmn = min(kmn, ck[j]); kmx = max(kmx, ck[j]); }
+    tk_minmax(kmn, kmx, sh);
+    tk_boundary<KPT>(ck, cvalid, m, k, kmn, kmx, sh, shift, hi, takeB);
+    tk_place<KPT>(ck, cvalid, shift, hi, takeB, sh,
+                  [&](int j, int pos) { s_row[pos] = c_page[tid * KPT + j]; }, tmin, nmax);
+    for (int x = tid; x < ng * k; x += kTkThreads) {
+        const int g = x / k, r = x - g * k;
+        sel[(int64_t)(bh + g) * kp + r] = s_row[r];
+    }
+    if (tid < ng) {
+        n_sel[bh + tid] = k;
+        if (aux) {
+            aux[2 * (bh + tid)] = key_float(tmin);
+            aux[2 * (bh + tid) + 1] = k < np ? key_float(max(nmax, out_next)) : -INFINITY;
+        }
+    }
+}
+
 // Phi(u) and phi(u) of the standard normal from one exponential: the tail
 // Phi(-x) = phi(x) R(x), x = |u|, with R the Mills ratio in the rational form
 // t P(t), t = 1 / (1 + x / 4) (coefficients fitted by gen_mills_ratio.py;
@@ -483,19 +858,101 @@ static int max_optin_smem() {
     return v;
 }
 
+template <int KPT, int PG>
+static cudaError_t launch_topk_reg(const float* bound, const KV& kv, int Hq, int kp,
+                                   int32_t* sel, int32_t* n_sel, float* aux, int gs, int units,
+                                   int csize, const WS& ws, const DecodeLayout& L,
+                                   cudaStream_t s) {
+    const int chunk = ((kv.maxp + csize - 1) / csize + 3) & ~3;   // as the kernel rounds
+    if (chunk > kTkThreads * KPT) return kShapeUnsupported;
+    const int slot = std::min(kp, chunk);
+    if (csize > 1 && csize * slot > kTkThreads * KPT) return kShapeUnsupported;
+    size_t smem = (size_t)kp * 4 + (csize > 1 ? (size_t)csize * slot * 8 : 0);
+    if (PG > 0)
+        smem += (size_t)PG * kp * 4 + (size_t)PG * ((kv.maxp + 31) / 32) * 4 + (size_t)L.Umax * 4;
+    if (smem > 96 * 1024) return kShapeUnsupported;
+    auto kernel = select_topk_reg_kernel<KPT, PG>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const int cl = PG > 1 && gs == 0 ? PG : csize;     // CTAs per cluster
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(units * csize);
+    cfg.blockDim = dim3(kTkThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cl > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, bound, kv, Hq, kp, sel, n_sel, aux, gs, csize, ws, L);
+}
+
+template <int KPT>
+static cudaError_t launch_topk_reg_plan(const float* bound, const KV& kv, int Hq, int kp,
+                                        int32_t* sel, int32_t* n_sel, float* aux, int gs,
+                                        int units, int csize, const WS* ws,
+                                        const DecodeLayout* L, bool* planned, cudaStream_t s) {
+    if (ws && csize == 1) {
+        const int G = Hq / kv.hkv;
+        cudaError_t e = kShapeUnsupported;
+        switch (G) {
+            case 1: e = launch_topk_reg<KPT, 1>(bound, kv, Hq, kp, sel, n_sel, aux, gs, units, 1, *ws, *L, s); break;
+            case 2: e = launch_topk_reg<KPT, 2>(bound, kv, Hq, kp, sel, n_sel, aux, gs, units, 1, *ws, *L, s); break;
+            case 4: e = launch_topk_reg<KPT, 4>(bound, kv, Hq, kp, sel, n_sel, aux, gs, units, 1, *ws, *L, s); break;
+            case 8: e = launch_topk_reg<KPT, 8>(bound, kv, Hq, kp, sel, n_sel, aux, gs, units, 1, *ws, *L, s); break;
+            default: break;
+        }
+        if (e != kShapeUnsupported) {
+            if (e == cudaSuccess) *planned = true;
+            return e;
+        }
+    }
+    return launch_topk_reg<KPT, 0>(bound, kv, Hq, kp, sel, n_sel, aux, gs, units, csize, WS{},
+                                   DecodeLayout{}, s);
+}
+
 cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp, int32_t* sel,
-                               int32_t* n_sel, float* aux, bool shared, cudaStream_t s) {
-    // shared: one CTA per (sequence, kv head), G times fewer CTAs, so each
-    // gets the most threads
+                               int32_t* n_sel, float* aux, bool shared, cudaStream_t s,
+                               void* plan_ws, const DecodeLayout* plan_layout, bool* planned) {
+    const int gs = shared ? Hq / kv.hkv : 0;
+    const int units = shared ? kv.B * kv.hkv : kv.B * Hq;
+    WS wsv{};
+    const WS* ws = nullptr;
+    if (plan_ws && plan_layout && planned) {
+        wsv = ws_views(plan_ws, *plan_layout);
+        ws = &wsv;
+        *planned = false;
+    }
+    // register-resident keys: at most 4096 pages per CTA, longer sequences
+    // split over a cluster of up to 8 CTAs
+    int csize = 1;
+    while (csize < kTkMaxCluster && (kv.maxp + csize - 1) / csize > 4096) csize *= 2;
+    const int chunk = ((kv.maxp + csize - 1) / csize + 3) & ~3;
+    cudaError_t e = kShapeUnsupported;
+    if (chunk <= kTkThreads * 4)
+        e = launch_topk_reg_plan<4>(bound, kv, Hq, kp, sel, n_sel, aux, gs, units, csize, ws,
+                                    plan_layout, planned, s);
+    else if (chunk <= kTkThreads * 8)
+        e = launch_topk_reg_plan<8>(bound, kv, Hq, kp, sel, n_sel, aux, gs, units, csize, ws,
+                                    plan_layout, planned, s);
+    if (e == kShapeUnsupported && chunk <= kTkThreads * 16)
+        e = launch_topk_reg_plan<16>(bound, kv, Hq, kp, sel, n_sel, aux, gs, units, csize, ws,
+                                     plan_layout, planned, s);
+    if (e != kShapeUnsupported) return e;
+
+    // large budgets: keys in shared memory, one CTA per head
     const int threads = shared ? 1024 : (kv.maxp <= 8192 ? 512 : 1024);
     const size_t smem = (size_t)kv.maxp * 4 + (size_t)kp * 4;
-    if ((int)smem > max_optin_smem() - 4096) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if ((int)smem > max_optin_smem() - 4096) return kShapeUnsupported;
+    e = cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
-    const int gs = shared ? Hq / kv.hkv : 0;
-    return launch_kernel(select_topk_kernel, dim3(shared ? kv.B * kv.hkv : kv.B * Hq), dim3(threads),
-                         smem, s, bound, kv, Hq, kp, sel, n_sel, aux, gs);
+    return launch_kernel(select_topk_kernel, dim3(units), dim3(threads), smem, s, bound, kv, Hq,
+                         kp, sel, n_sel, aux, gs);
 }
 
 cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, float alpha,
@@ -503,7 +960,7 @@ cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, 
                                 cudaStream_t s) {
     const int threads = kSelThreads;
     const size_t smem = (size_t)(threads / 32) * 256 * 4 + 256 * 4 + (size_t)kv.maxp * 16;
-    if ((int)smem > max_optin_smem() - 1024) return cudaErrorInvalidValue;
+    if ((int)smem > max_optin_smem() - 1024) return kShapeUnsupported;
     const bool e2 = fabsf(alpha - 1.5f) < 1e-6f;
     cudaError_t e;
     if (e2) {

@@ -22,6 +22,7 @@ EKV_UNSUPPORTED = 2
 EKV_WORKSPACE_TOO_SMALL = 3
 EKV_CUDA_ERROR = 4
 EKV_DEVICE_CHECK_FAILED = 5
+EKV_DEVICE_TIMEOUT = 6
 EKV_F32 = 0
 EKV_BF16 = 1
 EKV_SELECT_TOPK = 0
@@ -34,7 +35,7 @@ SYMBOLS = ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select"
            "entmaxkv_decode_counts", "entmaxkv_decode_noalloc", "entmaxkv_decode_full",
            "entmaxkv_full_workspace_size", "entmaxkv_decode_softmax",
            "entmaxkv_decode_softmax_full", "entmaxkv_softmax_workspace_size",
-           "entmaxkv_kept_mass")
+           "entmaxkv_kept_mass", "entmaxkv_check_wait_timeout", "entmaxkv_select_decode")
 
 
 class EntmaxKVError(RuntimeError):
@@ -88,11 +89,15 @@ def lib() -> C.CDLL:
         L.entmaxkv_kept_mass.argtypes = [vp] + [i32] * 7 + [f32, vp, vp, vp]
         L.entmaxkv_softmax_workspace_size.argtypes = [i32] * 7
         L.entmaxkv_softmax_workspace_size.restype = sz
+        L.entmaxkv_check_wait_timeout.argtypes = [C.c_uint32, vp]
+        L.entmaxkv_select_decode.argtypes = [vp, vp, i32, f32, vp, i32, i32, f32, f32, vp, vp,
+                                             vp, vp, vp, vp, vp, sz, vp]
         for name in ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select",
                      "entmaxkv_decode", "entmaxkv_read_device_status",
                      "entmaxkv_set_stage_events", "entmaxkv_decode_counts", "entmaxkv_decode_noalloc",
                      "entmaxkv_decode_full", "entmaxkv_decode_softmax",
-                     "entmaxkv_decode_softmax_full", "entmaxkv_kept_mass"):
+                     "entmaxkv_decode_softmax_full", "entmaxkv_kept_mass",
+                     "entmaxkv_check_wait_timeout", "entmaxkv_select_decode"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -294,6 +299,35 @@ def entmaxkv_decode(q: torch.Tensor, num_q_heads: int, scale: float, kv: PagedKV
                                  _stream(stream)))
 
 
+def entmaxkv_select_decode(page_scores: torch.Tensor, q: torch.Tensor, num_q_heads: int,
+                           scale: float, kv: PagedKV, policy: int, budget_tokens: int,
+                           alpha: float, delta: float, sel: torch.Tensor, n_sel: torch.Tensor,
+                           aux: torch.Tensor | None, out: torch.Tensor,
+                           tau_out: torch.Tensor | None, support_out: torch.Tensor | None,
+                           workspace: torch.Tensor, stream=None) -> None:
+    """entmaxkv_select then entmaxkv_decode in one call (the selection also
+    builds the decode's page union for the top-k policies)."""
+    cap = budget_tokens // kv.page_size
+    _need(page_scores, "page_scores", torch.float32)
+    _need(q, "q", torch.float32, (kv.batch, num_q_heads, kv.head_dim))
+    _need(sel, "sel", torch.int32, (kv.batch, num_q_heads, cap))
+    _need(n_sel, "n_sel", torch.int32, (kv.batch, num_q_heads))
+    if aux is not None:
+        _need(aux, "aux", torch.float32, (kv.batch, num_q_heads, 2))
+    _need(out, "out", torch.float32, (kv.batch, num_q_heads, kv.head_dim))
+    if tau_out is not None:
+        _need(tau_out, "tau_out", torch.float32, (kv.batch, num_q_heads))
+    if support_out is not None:
+        _need(support_out, "support_out", torch.int32, (kv.batch, num_q_heads))
+    _need(workspace, "workspace", torch.uint8)
+    _check("entmaxkv_select_decode",
+           lib().entmaxkv_select_decode(_ptr(page_scores), _ptr(q), num_q_heads, float(scale),
+                                        kv.ref, policy, budget_tokens, float(alpha),
+                                        float(delta), _ptr(sel), _ptr(n_sel), _ptr(aux),
+                                        _ptr(out), _ptr(tau_out), _ptr(support_out),
+                                        _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
 def entmaxkv_full_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, page_size,
                                  max_pages) -> int:
     return int(lib().entmaxkv_full_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
@@ -366,6 +400,14 @@ def entmaxkv_read_device_status(stream=None) -> int:
     _check("entmaxkv_read_device_status",
            lib().entmaxkv_read_device_status(C.byref(st), _stream(stream)))
     return int(st.value)
+
+
+def entmaxkv_check_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the library's self-check whose bounded wait runs out after
+    limit_us microseconds; entmaxkv_read_device_status then reports
+    EKV_DEVICE_TIMEOUT."""
+    _check("entmaxkv_check_wait_timeout",
+           lib().entmaxkv_check_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def entmaxkv_set_stage_events(events: list | None) -> None:

@@ -43,6 +43,7 @@ def test_status_strings_and_version(L):
     assert L.entmaxkv_status_string(0) == "ok"
     assert "workspace" in L.entmaxkv_status_string(3)
     assert L.entmaxkv_status_string(99) == "unknown status"
+    assert "timeout" in L.entmaxkv_status_string(L.EKV_DEVICE_TIMEOUT)
     assert L.entmaxkv_version() >= 10000
 
 
@@ -121,6 +122,9 @@ def test_invalid_arguments_are_rejected_before_any_launch(L):
     assert lib.entmaxkv_build_page_meta(ref, 0, 4, C.byref(empty), 0, 0,
                                         None) == L.EKV_INVALID_ARG
     assert lib.entmaxkv_read_device_status(None, None) == L.EKV_INVALID_ARG
+    # wait self-check: the limit must be 1 .. 100000 us
+    assert lib.entmaxkv_check_wait_timeout(0, None) == L.EKV_INVALID_ARG
+    assert lib.entmaxkv_check_wait_timeout(100001, None) == L.EKV_INVALID_ARG
     # full-cache decode: same checks as decode, no selection
     assert lib.entmaxkv_decode_full(nz, 1, 1.0, None, 1.5, nz, None, None, C.c_void_p(256),
                                     1 << 30, None) == L.EKV_INVALID_ARG

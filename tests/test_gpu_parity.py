@@ -426,6 +426,61 @@ def test_bad_page_table_entry_is_flagged_not_faulted():
     assert E.entmaxkv_read_device_status() == E.EKV_OK     # read clears it
 
 
+@pytest.mark.parametrize("name,over", [
+    ("long128k", {"batch": 2, "seq_lens": [16384, 12345]}),
+    ("long128k", {"batch": 2, "seq_lens": [16384, 12345], "policy": "topk_shared"}),
+    ("long128k", {"batch": 3, "seq_lens": [3000, 0, 77], "num_q_heads": 16, "num_kv_heads": 2,
+                  "planted_pages": 2}),
+    ("long128k", {"batch": 2, "seq_lens": [3000, 2049], "num_q_heads": 8, "num_kv_heads": 8,
+                  "dtype": "f32", "budget_tokens": 512, "planted_pages": 2}),
+    ("gauss64k", {"batch": 2, "seq_lens": [16384, 9999]}),
+    ("ctx1m", {"context": 262144}),
+])
+def test_select_decode_matches_the_separate_calls(name, over):
+    """entmaxkv_select_decode (the selection builds the decode's page union:
+    per-head clusters, shared selections, groups of 1 to 8, empty sequences;
+    Gaussian selection and long contexts keep the decode's own plan) returns,
+    bit for bit, what entmaxkv_select followed by entmaxkv_decode returns."""
+    w = make_workload(name, **over)
+    g = GpuRun(w)
+    d = g.dec
+    d.score(g.q)
+    d.select()
+    d.decode(g.q)
+    torch.cuda.synchronize()
+    names = ("n_sel", "aux", "out", "tau", "support")
+    ref = {k: getattr(d, k).clone() for k in names + ("sel",)}
+    for k in names + ("sel",):
+        getattr(d, k).fill_(-7)
+    d.select_decode(g.q)
+    torch.cuda.synchronize()
+    for k in names:
+        assert torch.equal(getattr(d, k), ref[k]), k
+    n = ref["n_sel"].cpu().numpy().reshape(-1)
+    a = d.sel.cpu().numpy().reshape(n.size, -1)
+    b = ref["sel"].cpu().numpy().reshape(n.size, -1)
+    for i in range(n.size):
+        assert np.array_equal(a[i, :n[i]], b[i, :n[i]]), i
+    assert E.entmaxkv_read_device_status() == E.EKV_OK
+
+
+def test_bounded_wait_timeout_is_reported_and_the_context_survives():
+    """The give-up path of the kernels' bounded waits: a wait on an mbarrier
+    that never completes runs out (1 ms limit), the kernel records a timeout
+    and returns; the status reads EKV_DEVICE_TIMEOUT once (the read clears it)
+    and a decode step afterwards still matches the oracle."""
+    import time
+    assert E.entmaxkv_read_device_status() == E.EKV_OK
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    E.entmaxkv_check_wait_timeout(1000)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 >= 1e-3
+    assert E.entmaxkv_read_device_status() == E.EKV_DEVICE_TIMEOUT
+    assert E.entmaxkv_read_device_status() == E.EKV_OK
+    full_parity(make_workload("long128k", batch=1, context=4096))
+
+
 def test_deterministic_across_runs():
     w = make_workload("long128k", batch=2, context=8192)
     g = GpuRun(w)

@@ -343,7 +343,7 @@ constexpr int kTkBins = 1 << kTkDigitBits;
 constexpr int kTkMaxCluster = 8;
 
 struct TkShared {
-    int hist[kTkBins];
+    int hist[2][kTkBins];            // one per radix pass, alternating (both zero between uses)
     int red[40];
     uint32_t umin[32], umax[32];
     int digit, above, nb;
@@ -399,46 +399,79 @@ __device__ __forceinline__ void tk_minmax(uint32_t& mn, uint32_t& mx, TkShared& 
 // The boundary of the k largest among this block's valid keys (bit j of
 // `valid` marks key[j]; 1 <= k <= the number of valid keys; kmn/kmx their
 // extremes).  Key x is taken iff (x >> shift) > hi, or (x >> shift) == hi and
-// fewer than takeB such keys precede it in key order.  sh.hist must be zero on
-// entry and is zero again on return.
+// fewer than takeB such keys precede it in key order.  Each radix pass costs
+// two barriers: the histogram (alternating buffers, so the other one is
+// cleared meanwhile), then warp 0 alone finds the boundary bin -- every lane
+// sums its 64 consecutive bins, a suffix scan over the lanes picks the lane
+// holding the boundary and the warp scans that lane's 64 bins.  Both
+// histograms are zero on entry and are zero again before the next barrier
+// the caller passes.
 template <int KPT>
 __device__ void tk_boundary(const uint32_t (&key)[KPT], uint32_t valid, int n, int k,
                             uint32_t kmn, uint32_t kmx, TkShared& sh, int& shift_out,
                             uint64_t& hi_out, int& takeB_out) {
-    constexpr int BPT = kTkBins / kTkThreads;          // bins per thread
-    const int tid = threadIdx.x;
+    constexpr int BPL = kTkBins / 32;                   // bins per lane of warp 0
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const uint32_t diff = kmn ^ kmx;
     int shift = diff ? 32 - __clz(diff) : 0;
     uint64_t hi = (uint64_t)kmx >> shift;
     int rem = k, nB = n;
+    int buf = 0;
+    bool used = false;
     while (shift > 0 && nB != rem) {
         const int dbits = min(kTkDigitBits, shift);
         shift -= dbits;
         const uint32_t dmask = (1u << dbits) - 1u;
+        int* hist = sh.hist[buf];
 #pragma unroll
         for (int j = 0; j < KPT; ++j)
             if (((valid >> j) & 1u) && ((uint64_t)key[j] >> (shift + dbits)) == hi)
-                atomicAdd(&sh.hist[(key[j] >> shift) & dmask], 1);
+                atomicAdd(&hist[(key[j] >> shift) & dmask], 1);
         __syncthreads();
-        int c[BPT], local = 0;
+        if (wid == 0) {
+            int sum = 0;                                 // lane's bins [lane BPL, +BPL), rotated
+#pragma unroll 16
+            for (int i = 0; i < BPL; ++i) sum += hist[lane * BPL + ((i + lane) & (BPL - 1))];
+            int incl = sum;                              // suffix sum over the lanes
 #pragma unroll
-        for (int b = 0; b < BPT; ++b) { c[b] = sh.hist[tid * BPT + b]; local += c[b]; }
-        int total;
-        const int pre = block_exclusive_scan(local, sh.red, &total);
-        int acc = total - pre - local;                  // keys in the bins above this thread's
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+                if (lane + o < 32) incl += v;
+            }
+            const int above_l = incl - sum;
+            const uint32_t owner = __ballot_sync(0xFFFFFFFFu, above_l < rem && incl >= rem);
+            const int L = __ffs(owner) - 1;              // exactly one lane
+            const int base = __shfl_sync(0xFFFFFFFFu, above_l, L);
+            // that lane's bins, two per lane, suffix-scanned
+            const int b0 = L * BPL + 2 * lane;
+            const int c0 = hist[b0], c1 = hist[b0 + 1];
+            int pair = c0 + c1, pin = pair;
 #pragma unroll
-        for (int b = BPT - 1; b >= 0; --b) {
-            if (acc < rem && acc + c[b] >= rem) { sh.digit = tid * BPT + b; sh.above = acc; sh.nb = c[b]; }
-            acc += c[b];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_down_sync(0xFFFFFFFFu, pin, o);
+                if (lane + o < 32) pin += v;
+            }
+            int acc = base + pin - pair;                 // keys above this lane's two bins
+            if (acc < rem && acc + c1 >= rem) { sh.digit = b0 + 1; sh.above = acc; sh.nb = c1; }
+            acc += c1;
+            if (acc < rem && acc + c0 >= rem) { sh.digit = b0; sh.above = acc; sh.nb = c0; }
+        } else if (used) {
+            // the other buffer, last read before the previous pass's second barrier
+            int* other = sh.hist[buf ^ 1];
+            for (int i = tid - 32; i < kTkBins; i += blockDim.x - 32) other[i] = 0;
         }
         __syncthreads();
         const int d = sh.digit;
         rem -= sh.above;
         nB = sh.nb;
         hi = (hi << dbits) | (uint64_t)d;
-#pragma unroll
-        for (int b = 0; b < BPT; ++b) sh.hist[tid * BPT + b] = 0;
-        __syncthreads();
+        buf ^= 1;
+        used = true;
+    }
+    // leave both buffers zero: the last one (read before the barrier above)
+    // and the other one if two or more passes ran
+    if (used) {
+        for (int i = tid; i < kTkBins; i += blockDim.x) sh.hist[buf ^ 1][i] = 0;
     }
     shift_out = shift;
     hi_out = hi;
@@ -564,7 +597,7 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     }
     if (csize > 1 || (PG > 1 && gs == 0)) cluster_arrive_relaxed();   // waited for before the first remote store
     const int n_loc = max(0, min(np - p0, chunk));
-    for (int i = tid; i < kTkBins; i += kTkThreads) sh.hist[i] = 0;
+    for (int i = tid; i < 2 * kTkBins; i += kTkThreads) (&sh.hist[0][0])[i] = 0;
 
     // this thread's keys: pages p0 + [tid KPT, (tid + 1) KPT)
     uint32_t key[KPT];

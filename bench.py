@@ -65,11 +65,13 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--mode", choices=["sparse", "full", "softmax", "softmax_full"],
+    ap.add_argument("--mode", choices=["sparse", "full", "softmax", "softmax_full", "meta"],
                     default="sparse",
                     help="sparse: the EntmaxKV step (headline); full: full-cache entmax decode; "
                          "softmax: softmax over the same kept pages; softmax_full: full-cache "
-                         "softmax")
+                         "softmax; meta: the page-metadata build (prefill) alone")
+    ap.add_argument("--cpu-1core", action="store_true",
+                    help="also time the oracle on one host thread (cpu_baseline_1core)")
     return ap.parse_args()
 
 
@@ -318,6 +320,56 @@ def oracle_full_time_per_step(w, seconds: float, steps: int = 1, mode: str = "fu
     return statistics.mean(times), desc, cores
 
 
+def selection_ties(w, sel, n_sel, heads, tie_rtol: float = 2e-5) -> dict:
+    """The GPU page selection of `heads` against the fp64 oracle's: heads with
+    the same page set, heads that differ only by pages whose oracle decision
+    score lies within tie_rtol (relative to the score's magnitude) of the
+    decision boundary, and heads that differ otherwise (a parity failure)."""
+    import numpy as np
+    import oracle
+    kv = oracle.KV(w)
+    meta = oracle.build_meta(kv)
+    r = oracle.sparse_step(kv, w, heads=np.asarray(heads, dtype=np.int32), meta=meta)
+    s = float(w.scale)
+    G = w.group
+    same = tied = other = 0
+    for bh in heads:
+        gs = set(sel[bh, :n_sel[bh]].tolist())
+        os_ = set(r["sel"][bh, :r["n_sel"][bh]].tolist())
+        if gs == os_:
+            same += 1
+            continue
+        b, h = divmod(bh, w.num_q_heads)
+        qa = np.abs(w.q[b, h].astype(np.float64))
+        ok = True
+        for p in gs ^ os_:
+            blk = w.page_table[b, p]
+            if w.policy == "gauss":
+                c = w.alpha - 1.0
+                mag = c * s * (np.abs(meta.mean[blk, h // G]) @ qa
+                               + np.sqrt(meta.var[blk, h // G] @ (qa * qa))) + 1e-6
+                zs = c * r["zmax"][bh]
+                np_ = w.pages_of(b)
+                passing = np.sort(zs[:np_][zs[:np_] >= r["tau_hat"][bh] - w.delta])[::-1]
+                bnd = (passing[w.cap_pages - 1] if len(passing) > w.cap_pages
+                       else r["tau_hat"][bh] - w.delta)
+                score = zs[p]
+            else:
+                amp = np.maximum(np.abs(meta.kmin[blk]), np.abs(meta.kmax[blk]))
+                gh = range(G) if w.policy == "topk_shared" else [h % G]
+                mag = max(s * (amp[h // G] @ np.abs(w.q[b, (h // G) * G + g].astype(np.float64)))
+                          for g in gh)
+                score = (r["shared"][bh, p] if w.policy == "topk_shared" else r["bound"][bh, p])
+                bnd = r["kth"][bh]
+            ok = ok and abs(score - bnd) <= tie_rtol * mag
+        if ok:
+            tied += 1
+        else:
+            other += 1
+    return {"heads_checked": len(heads), "identical": same, "ties_at_boundary": tied,
+            "other_differences": other, "tie_window": f"{tie_rtol:g} of the score magnitude"}
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -497,9 +549,22 @@ def run_ours(args):
                          "H2D of q, the step's kernels and the D2H of out) and the sync"}
 
     cpu = None
+    ties = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, desc, cores, _ = oracle_time_per_step(w, args.cpu_seconds)
         cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc}
+        import numpy as np
+        BH = w.batch * w.num_q_heads
+        sample = np.sort(np.random.default_rng(5).choice(BH, size=min(BH, 32), replace=False))
+        ties = selection_ties(w, dec.sel.cpu().numpy().reshape(BH, -1),
+                              dec.n_sel.cpu().numpy().reshape(BH), sample.tolist())
+        if args.cpu_1core:
+            import oracle
+            nthreads = oracle.get_threads()
+            oracle.set_threads(1)
+            us1, desc1, _, _ = oracle_time_per_step(w, args.cpu_seconds, steps=2)
+            oracle.set_threads(nthreads)
+            cpu["one_core"] = {"value": us1, "unit": "us/step", "cores": 1, "sample": desc1}
 
     if world > 1:
         dist.barrier()
@@ -521,7 +586,7 @@ def run_ours(args):
                             "v_support_rows": bytes_v, "q_and_out": small,
                             "union_pages": int(up.sum()), "v_rows": int(vr.sum())},
         "stage_us": {n: v * 1e3 for n, v in mean.items()},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "selection": ties,
         "gpu_launches": kernels_per_step(w) * K, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -702,10 +767,93 @@ def run_full(args):
         dist.destroy_process_group()
 
 
+def run_meta(args):
+    """The page-metadata build of the whole cache (kmin/kmax for the bound
+    policies, mean/var for the Gaussian one), timed like the step: a CUDA
+    graph of one entmaxkv_build_page_meta call, L2 flushed between calls.
+    Bytes: the valid K pages read, the metadata written, the page table."""
+    import torch
+    import torch.distributed as dist
+
+    from sparse_long_context_08_b300 import entmaxkv as E
+    from sparse_long_context_08_b300.api import EntmaxKVDecoder, upload_workload
+    from sparse_long_context_08_b300.workloads import make_workload
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    E.lib()
+    w = make_workload(args.workload, seed=rank_seed(args.workload, rank), **overrides(args))
+    kv, q = upload_workload(w)
+    dec = EntmaxKVDecoder(kv, w.num_q_heads, float(w.scale), w.alpha, w.policy,
+                          w.budget_tokens, w.delta)
+    torch.cuda.synchronize()
+    flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device="cuda")
+    flush_read = torch.ones(max(1, args.flush_mb // 2) << 20, dtype=torch.uint8, device="cuda")
+
+    def flush_l2(i):
+        flush.fill_(i & 255)
+        flush_read.sum(dtype=torch.int32)
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap_stream):
+        for _ in range(2):
+            dec.build_meta(stream=cap_stream)
+    torch.cuda.current_stream().wait_stream(cap_stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap_stream):
+        dec.build_meta(stream=cap_stream)
+    for i in range(max(3, args.warmup)):
+        graph.replay()
+        flush_l2(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(bus_id_of(local_rank)) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    K = args.steps
+    total = timed_replays(graph, K, flush_l2)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(sum(total), world, "cuda") / K
+    esz = 2 if w.dtype == "bf16" else 4
+    pages = sum(w.pages_of(b) for b in range(w.batch))
+    gauss = w.policy == "gauss"
+    bytes_k = sum(int(w.seq_lens[b]) for b in range(w.batch)) * w.num_kv_heads * w.head_dim * esz
+    bytes_meta = pages * w.num_kv_heads * 2 * w.head_dim * (4 if gauss else esz)
+    bytes_all = bytes_k + bytes_meta + pages * 4
+    peak, peak_kind = measured_peak()
+    gbs = bytes_all / (ms * 1e-3) / 1e9
+    if rank == 0:
+        line = {"metric": "page-metadata build us and achieved HBM GB/s (frac of peak)",
+                "value": whole_job_us_per_step(ms, world), "unit": "us/build", "n_gpus": world,
+                "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms,
+                "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32" if gauss else w.dtype, "data": "synthetic",
+                "config": dict(workload_config(w), mode="meta",
+                               statistics="mean/var" if gauss else "kmin/kmax"),
+                "hbm_gbs": gbs, "hbm_frac_of_measured": gbs / peak, "hbm_frac_of_8tbs": gbs / 8000.0,
+                "bytes_per_step": bytes_all,
+                "bytes_breakdown": {"k_read": bytes_k, "metadata_written": bytes_meta,
+                                    "page_table": pages * 4},
+                "roofline": {"bound": "hbm", "kernel": "build_meta", "achieved": gbs, "peak": peak,
+                             "unit": "GB/s", "frac": gbs / peak,
+                             "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                             "algorithmic_bytes": bytes_all},
+                "cpu_baseline": None, "e2e": None, "gpu_launches": K, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.mode == "meta":
+        run_meta(args)
     elif args.mode != "sparse":
         run_full(args)
     else:

@@ -17,3 +17,20 @@ def oracle_lib():
     import oracle
     oracle.lib()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Selection ties of the GPU parity tests: heads whose page set differs from
+    the oracle's only by pages whose fp64 score is within the tie window of the
+    decision boundary."""
+    try:
+        from gpu_util import TIES
+    except Exception:
+        return
+    if not TIES:
+        return
+    heads = sum(n for _, n, _ in TIES)
+    ties = sum(t for _, _, t in TIES)
+    terminalreporter.write_line(
+        f"selection ties: {ties} of {heads} compared heads differ from the oracle only at the "
+        f"decision boundary ({sum(1 for _, _, t in TIES if t)} of {len(TIES)} comparisons)")

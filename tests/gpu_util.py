@@ -151,6 +151,43 @@ def compare_selection(w, g_sel, g_n, o_sel, o_n, score, mag, boundary, heads):
     return ties
 
 
+# Heads whose GPU page selection differs from the oracle's only by pages tied at
+# the decision boundary, per test (printed at the end of the session).
+TIES: list[tuple[str, int, int]] = []
+
+
+def record_ties(name: str, heads: int, ties: int) -> None:
+    TIES.append((name, heads, ties))
+
+
+def selected_scores(w, sel, n_sel, bh):
+    """fp64 z' = (alpha - 1) s q.k of every valid token of head bh's selected
+    pages (K widened exactly)."""
+    b, h = divmod(bh, w.num_q_heads)
+    pages = sel[bh, :n_sel[bh]]
+    K = w.k_pool[w.page_table[b, pages], h // w.group]          # [n, P, d]
+    K = bf16_bits_to_f32(K) if w.dtype == "bf16" else K
+    q = w.q[b, h].astype(np.float64)
+    z = [K[j, :min(w.page_size, int(w.seq_lens[b]) - int(p) * w.page_size)].astype(np.float64) @ q
+         for j, p in enumerate(pages)]
+    z = np.concatenate(z) if z else np.zeros(0)
+    return (w.alpha - 1.0) * float(w.scale) * z
+
+
+def compare_support(w, sel, n_sel, g_sup, o_sup, o_tau, heads):
+    """Support sizes (#{p > 0}) agree, except by tokens whose fp64 score lies
+    within the tau tolerance band of the oracle's tau: only such a token can
+    change sides between the fp32 and the fp64 threshold."""
+    for bh in heads:
+        if int(g_sup[bh]) == int(o_sup[bh]):
+            continue
+        assert np.isfinite(o_tau[bh]), (bh, g_sup[bh], o_sup[bh])
+        zp = selected_scores(w, sel, n_sel, bh)
+        band = TAU_RTOL * max(abs(o_tau[bh]), 1.0)
+        near = int(np.sum(np.abs(zp - o_tau[bh]) <= band))
+        assert abs(int(g_sup[bh]) - int(o_sup[bh])) <= near, (bh, g_sup[bh], o_sup[bh], near)
+
+
 def compare_decode(g_out, g_tau, o_out, o_tau, heads, g_sup=None, o_sup=None):
     for bh in heads:
         if np.isinf(o_tau[bh]):

@@ -12,7 +12,7 @@ from sparse_long_context_08_b300 import entmaxkv as E
 from sparse_long_context_08_b300.workloads import make_workload
 
 from gpu_util import (GpuRun, bbox_scale, compare_decode, compare_meta, compare_scores,
-                      compare_selection, gauss_scale)
+                      compare_selection, compare_support, gauss_scale, record_ties)
 
 pytestmark = pytest.mark.gpu
 
@@ -80,7 +80,8 @@ def full_parity(w, heads=None, check_e2e=True):
     # decode on the oracle's own selection
     g_out, g_tau, g_sup = g.decode_with(osel, on)
     o_out, o_tau, o_sup, o_psum = oracle.decode_sparse(kv, s, w.alpha, osel, on, heads=hs)
-    compare_decode(g_out, g_tau, o_out, o_tau, hs, g_sup, o_sup)
+    compare_decode(g_out, g_tau, o_out, o_tau, hs)
+    compare_support(w, osel, on, g_sup, o_sup, o_tau, hs)
     # end to end: where the two selections agree, the outputs agree
     if check_e2e:
         same = [bh for bh in hs if r["n_sel"][bh] == on[bh]
@@ -89,6 +90,7 @@ def full_parity(w, heads=None, check_e2e=True):
         compare_decode(r["out"], r["tau"], o_out, o_tau, same)
     assert E.entmaxkv_read_device_status() == E.EKV_OK
     rep["support"] = o_sup
+    record_ties(w.name, len(hs), rep["ties"])
     return rep
 
 
@@ -317,7 +319,8 @@ def test_discarded_mass_full_size_sampled_heads():
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (8, 1), (16, 4), (32, 4), (64, 8)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (8, 1), (16, 4), (32, 4), (16, 8),
+                                     (64, 8)])
 def test_shapes(d, dtype, hq, hkv):
     w = make_workload("long128k", batch=2, seq_lens=[3000, 2049], head_dim=d, dtype=dtype,
                       num_q_heads=hq, num_kv_heads=hkv, page_size=16, budget_tokens=512,

@@ -296,6 +296,33 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Programmatic dependent launch: a kernel launched with launch_kernel_pdl may
+// start while the previous kernel in the stream is still running; it calls
+// pdl_wait() before its first read of that kernel's output (the wait returns
+// once the previous grid has completed and its memory is visible; without the
+// launch attribute it returns at once).  A kernel calls pdl_trigger() when its
+// main work is done, so that the next kernel's CTAs can be placed on SMs it
+// frees while its last CTAs finish.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // L2 policy for data read once (the K/V pools and page metadata streams): the
 // lines are the first to go, so the small per-step arrays written between the
 // kernels (bounds, scores) stay in L2 for the next kernel.

@@ -444,6 +444,7 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
     unsigned char* ring = s_qm + (size_t)warp * ns * page_bytes;
     int* s_prefix = reinterpret_cast<int*>(s_qm + (size_t)kQmWarps * ns * page_bytes);
     uint64_t* bar = s_bar[warp];
+    pdl_wait();                 // the union plan is the previous kernel's output
     {
         const int U = L.U;
         const int seg = (U + blockDim.x - 1) / blockDim.x;
@@ -608,6 +609,7 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
         hm = fmaxf(hm, pgm);
         __syncwarp();        // every lane is done with stage st before it is refilled
     }
+    pdl_trigger();
     if (failed) {
         if (lane == 0) flag_timeout();
         return;
@@ -911,6 +913,7 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
     float* outb = out + (int64_t)bh * D;
 
     // 1. the union size and the head's per-page maxima
+    pdl_wait();                               // the scores are the previous kernel's output
     const int ucnt = __ldcg(ws.union_count + u);
     float pm[kTpvPmVec];
 #pragma unroll
@@ -1607,7 +1610,7 @@ static cudaError_t launch_tpv(float alpha, int Hq, const KV& kv, const WS& ws,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     stage_mark(2, s);
-    e = launch_kernel(tpv_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvThreads), smem, s, Hq, alpha,
+    e = launch_kernel_pdl(tpv_kernel<T, D, E>, dim3(kv.B * Hq), dim3(kTpvThreads), smem, s, Hq, alpha,
                       cand_cap, kv, ws, L, out, tau_out, support_out);
     if (e != cudaSuccess) return e;
     stage_mark(3, s);
@@ -1629,7 +1632,7 @@ static cudaError_t launch_qk(const float* q, int Hq, float qscale, const KV& kv,
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         stage_mark(1, s);
-        e = launch_kernel(kernel, dim3(sm_count() * kQmCtasPerSm), dim3(kQmWarps * 32), smem, s, q, Hq,
+        e = launch_kernel_pdl(kernel, dim3(sm_count() * kQmCtasPerSm), dim3(kQmWarps * 32), smem, s, q, Hq,
                           qscale, kv, ws, L, ns);
         if (e != cudaSuccess) return e;
     } else {

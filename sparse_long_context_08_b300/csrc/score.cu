@@ -336,18 +336,15 @@ struct TcSh {
     int abort;
 };
 
-// Tile t (< tprefix[B]) -> sequence, first page, pages in the tile.
+// Tile t (< B * tps, tps = ceil(max_pages / PPT) tiles per sequence) ->
+// sequence, first page, pages of the sequence in the tile (<= 0: none).  The
+// fixed number of tiles per sequence lets a CTA find its tiles without the
+// sequence lengths, so its first page-table loads need not wait for them.
 template <int PPT>
-__device__ __forceinline__ void tc_tile(int t, const int* tprefix, const KV& kv, int& b, int& p0,
-                                        int& npg) {
-    int lo = 0, hi = kv.B - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tprefix[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-    const int np = min(kv.maxp, (kv.sl[b] + kv.P - 1) / kv.P);
-    p0 = (t - tprefix[b]) * PPT;
+__device__ __forceinline__ void tc_tile(int t, int tps, const KV& kv, int& b, int& p0, int& npg) {
+    b = t / tps;
+    p0 = (t - b * tps) * PPT;
+    const int np = min(kv.maxp, (__ldg(kv.sl + b) + kv.P - 1) / kv.P);
     npg = min(PPT, np - p0);
 }
 
@@ -422,29 +419,10 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
     unsigned char* bbuf = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     unsigned char* ring = bbuf + C::B_BYTES;
-    int* tprefix = reinterpret_cast<int*>(ring + (size_t)S * C::A_BYTES);   // [B + 1]
     __shared__ TcSh sh;
-    __shared__ int red[40];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tps = (kv.maxp + PPT - 1) / PPT;       // tiles per sequence
 
-    {   // tiles per sequence: ceil(pages / PPT)
-        const int B = kv.B;
-        const int seg = (B + blockDim.x - 1) / blockDim.x;
-        const int a0 = min(B, tid * seg), a1 = min(B, a0 + seg);
-        auto tiles_of = [&](int x) {
-            const int np = min(kv.maxp, (kv.sl[x] + kv.P - 1) / kv.P);
-            return (np + PPT - 1) / PPT;
-        };
-        int c = 0;
-        for (int x = a0; x < a1; ++x) c += tiles_of(x);
-        int tot;
-        int run = block_exclusive_scan(c, red, &tot);
-        for (int x = a0; x < a1; ++x) {
-            tprefix[x] = run;
-            run += tiles_of(x);
-        }
-        if (tid == 0) tprefix[B] = tot;
-    }
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&sh.full[i], kTcProd);
@@ -461,7 +439,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem;
-    const int total = tprefix[kv.B];
+    const int total = kv.B * tps;
     const int t0 = (int)((int64_t)total * blockIdx.x / gridDim.x);
     const int t1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
     const int nt = t1 - t0;
@@ -481,11 +459,15 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
         constexpr int kNoPage = INT_MIN;               // lane without a page in the tile
         // tile i: its sequence (returned) and this lane's page table entry
         auto page_block = [&](int i, int& blk) {
-            int b, p0, npg;
-            tc_tile<PPT>(t0 + i, tprefix, kv, b, p0, npg);
-            blk = kNoPage;
-            if (lane < PPW && warp * PPW + lane < npg)
-                blk = __ldg(kv.pt + (int64_t)b * kv.maxp + p0 + warp * PPW + lane);
+            const int t = t0 + i;
+            const int b = t / tps;
+            const int p = (t - b * tps) * PPT + warp * PPW + lane;
+            // the entry (inside the table row) is loaded with the sequence
+            // length; it is kept only for a page of the sequence
+            const int e = (lane < PPW && p < kv.maxp) ? __ldg(kv.pt + (int64_t)b * kv.maxp + p) : 0;
+            int bb, p0, npg;
+            tc_tile<PPT>(t, tps, kv, bb, p0, npg);
+            blk = (lane < PPW && warp * PPW + lane < npg) ? e : kNoPage;
             return b;
         };
         auto checked = [&](int blk) {
@@ -591,7 +573,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
         const int col0 = (quarter * 32 / PPT) * 3 * G;
         if (nt > 0) {                                  // B of the first tile's sequence
             int b, p0, npg;
-            tc_tile<PPT>(t0, tprefix, kv, b, p0, npg);
+            tc_tile<PPT>(t0, tps, kv, b, p0, npg);
             tc_build_b<D, G, HKV, 128>(bbuf, q, scale, b, tid - (kTcMmaWarp + 1) * 32);
             fence_proxy_async_smem();
             mbar_arrive(&sh.binit);
@@ -612,7 +594,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
             tc_fence_before();
             mbar_arrive(&sh.acce[a]);
             int b, p0, npg;
-            tc_tile<PPT>(t0 + i, tprefix, kv, b, p0, npg);
+            tc_tile<PPT>(t0 + i, tps, kv, b, p0, npg);
             if (pi < npg) {
                 const int p = p0 + pi;
                 const int blk = __ldg(kv.pt + (int64_t)b * kv.maxp + p);
@@ -631,6 +613,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
             }
         }
     }
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == kTcMmaWarp) {
@@ -647,7 +630,7 @@ static cudaError_t launch_score_tc_t(const float* q, float scale, const KV& kv, 
     if (kv.B > kTcMaxSeqs || (reinterpret_cast<uintptr_t>(kmin) & 15) ||
         (reinterpret_cast<uintptr_t>(kmax) & 15))
         return cudaErrorNotSupported;
-    const size_t smem = 1024 + C::B_BYTES + (size_t)C::S * C::A_BYTES + (size_t)(kv.B + 1) * sizeof(int);
+    const size_t smem = 1024 + C::B_BYTES + (size_t)C::S * C::A_BYTES;
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||

@@ -551,6 +551,7 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     const int p0 = (int)rank * chunk;
     const int span = max(0, min(kv.maxp - p0, chunk));
     const float* src = bound + (int64_t)bh * kv.maxp + p0;
+    pdl_wait();                         // the bounds are the previous kernel's output
     float v[KPT];
     {
         const bool vec = (kv.maxp & 3) == 0;
@@ -624,6 +625,7 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
         tk_place<KPT>(key, valid, shift, hi, takeB, sh,
                       [&](int j, int pos) { s_row[pos] = tid * KPT + j; }, tmin, nmax);
         // tk_place ends with a barrier: s_row is complete
+        pdl_trigger();
         for (int x = tid; x < ng * k; x += kTkThreads) {
             const int g = x / k, r = x - g * k;
             sel[(int64_t)(bh + g) * kp + r] = s_row[r];
@@ -683,6 +685,7 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
         st_cluster_u32(&sh.next[rank], 0u, k_loc < n_loc ? nmax : 0u);
     }
     cluster_sync_all();                 // candidates visible in the rank-0 CTA
+    pdl_trigger();
     if (rank != 0) return;              // nothing reads another CTA's memory past here
 
     // rank 0: the k best of the candidates; flat position x = r * slot + i
@@ -914,13 +917,15 @@ static cudaError_t launch_topk_reg(const float* bound, const KV& kv, int Hq, int
     cfg.blockDim = dim3(kTkThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cl;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = cl > 1 ? 1 : 0;
+    cfg.numAttrs = cl > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, bound, kv, Hq, kp, sel, n_sel, aux, gs, csize, ws, L);
 }
 

@@ -323,6 +323,15 @@ inline cudaError_t launch_kernel_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 b
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// cp.async of 16 bytes global -> shared, of which src_bytes (0 or 16) are
+// read and the rest zero-filled; cp_async_wait_all waits for all of this
+// thread's copies.
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // L2 policy for data read once (the K/V pools and page metadata streams): the
 // lines are the first to go, so the small per-step arrays written between the
 // kernels (bounds, scores) stay in L2 for the next kernel.

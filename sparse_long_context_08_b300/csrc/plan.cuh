@@ -50,12 +50,81 @@ inline size_t plan_smem_bytes(int G, int max_pages, int Umax, int cap) {
     return (size_t)G * ((max_pages + 31) / 32) * 4 + (size_t)Umax * 4 + (size_t)G * cap * 4;
 }
 
+// The union plan of unit u = (sequence b, kv head) from its G heads' page
+// bitmaps s_bits ([G][nwm] words, nwm = ceil(max_pages / 32); words past the
+// sequence's pages are not read): the ascending union of the pages, each
+// page's head mask and physical block, and the union size.  Called by every
+// thread of the block; `red` >= 40 ints.  s_pblk (nullable): the sequence's
+// page-table row in shared memory; without it the blocks are read from the
+// page table in global memory, and s_upage ([Umax]) is scratch.  Entries
+// outside [0, num_blocks) are flagged and planned as -1.
+template <int G>
+__device__ void plan_from_bits(const KV& kv, const WS& ws, const DecodeLayout& L, int u,
+                               const uint32_t* s_bits, int* s_upage, int* red,
+                               const int* s_pblk = nullptr) {
+    const int nwm = (kv.maxp + 31) / 32;
+    const int b = u / kv.hkv;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int nw = (pages_of(kv, b) + 31) / 32;
+    const int seg = (nw + nt - 1) / nt;
+    const int w0 = min(nw, tid * seg), w1 = min(nw, w0 + seg);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) {
+        uint32_t x = 0;
+#pragma unroll
+        for (int h = 0; h < G; ++h) x |= s_bits[h * nwm + w];
+        cnt += __popc(x);
+    }
+    int total;
+    int idx = block_exclusive_scan(cnt, red, &total);
+    int* upage = ws.union_page + (int64_t)u * L.Umax;
+    int* umask = ws.union_mask + (int64_t)u * L.Umax;
+    int* ublk = ws.union_blk + (int64_t)u * L.Umax;
+    for (int w = w0; w < w1; ++w) {
+        uint32_t hw[G];
+        uint32_t uw = 0;
+#pragma unroll
+        for (int h = 0; h < G; ++h) { hw[h] = s_bits[h * nwm + w]; uw |= hw[h]; }
+        while (uw) {
+            const int bit = __ffs(uw) - 1;
+            uw &= uw - 1;
+            int mask = 0;
+#pragma unroll
+            for (int h = 0; h < G; ++h) mask |= static_cast<int>((hw[h] >> bit) & 1u) << h;
+            upage[idx] = w * 32 + bit;
+            umask[idx] = mask;
+            if (s_pblk) {
+                int blk = s_pblk[w * 32 + bit];
+                if (blk < 0 || blk >= kv.nb) {
+                    flag_bad_data();
+                    blk = -1;
+                }
+                ublk[idx] = blk;
+            } else {
+                s_upage[idx] = w * 32 + bit;
+            }
+            ++idx;
+        }
+    }
+    if (tid == 0) ws.union_count[u] = total;
+    if (s_pblk) return;
+    __syncthreads();
+    // physical blocks of the union pages (one parallel page-table round trip)
+    for (int i = tid; i < total; i += nt) {
+        int blk = kv.pt[(int64_t)b * kv.maxp + s_upage[i]];
+        if (blk < 0 || blk >= kv.nb) {
+            flag_bad_data();
+            blk = -1;
+        }
+        ublk[i] = blk;
+    }
+}
+
 // The union plan of unit u from its G heads' selection rows already in
 // shared memory (s_sel [G][cap], s_ns [G] counts, each in [0, cap]): the
-// ascending union of the pages, each page's head mask and physical block, and
-// the union size.  Called by every thread of the block; s_bits ([G][nwm]
-// words) and s_upage ([Umax]) are scratch; `red` >= 40 ints.  Pages outside
-// the sequence are skipped and flagged.
+// rows are set into the bitmaps s_bits ([G][nwm] words, scratch), then
+// plan_from_bits.  s_upage ([Umax]) is scratch; `red` >= 40 ints.  Pages
+// outside the sequence are skipped and flagged.
 template <int G>
 __device__ void plan_from_rows(const KV& kv, int cap, const WS& ws, const DecodeLayout& L, int u,
                                const int* s_sel, const int* s_ns, uint32_t* s_bits, int* s_upage,
@@ -79,49 +148,7 @@ __device__ void plan_from_rows(const KV& kv, int cap, const WS& ws, const Decode
         }
     }
     __syncthreads();
-
-    const int seg = (nw + nt - 1) / nt;
-    const int w0 = min(nw, tid * seg), w1 = min(nw, w0 + seg);
-    int cnt = 0;
-    for (int w = w0; w < w1; ++w) {
-        uint32_t x = 0;
-#pragma unroll
-        for (int h = 0; h < G; ++h) x |= s_bits[h * nwm + w];
-        cnt += __popc(x);
-    }
-    int total;
-    int idx = block_exclusive_scan(cnt, red, &total);
-    int* upage = ws.union_page + (int64_t)u * L.Umax;
-    int* umask = ws.union_mask + (int64_t)u * L.Umax;
-    for (int w = w0; w < w1; ++w) {
-        uint32_t hw[G];
-        uint32_t uw = 0;
-#pragma unroll
-        for (int h = 0; h < G; ++h) { hw[h] = s_bits[h * nwm + w]; uw |= hw[h]; }
-        while (uw) {
-            const int bit = __ffs(uw) - 1;
-            uw &= uw - 1;
-            int mask = 0;
-#pragma unroll
-            for (int h = 0; h < G; ++h) mask |= static_cast<int>((hw[h] >> bit) & 1u) << h;
-            upage[idx] = w * 32 + bit;
-            umask[idx] = mask;
-            s_upage[idx] = w * 32 + bit;
-            ++idx;
-        }
-    }
-    __syncthreads();
-    // physical blocks of the union pages (one parallel page-table round trip)
-    int* ublk = ws.union_blk + (int64_t)u * L.Umax;
-    for (int i = tid; i < total; i += nt) {
-        int blk = kv.pt[(int64_t)b * kv.maxp + s_upage[i]];
-        if (blk < 0 || blk >= kv.nb) {
-            flag_bad_data();
-            blk = -1;
-        }
-        ublk[i] = blk;
-    }
-    if (tid == 0) ws.union_count[u] = total;
+    plan_from_bits<G>(kv, ws, L, u, s_bits, s_upage, red);
 }
 
 // Resets unit u's per-call state: its heads' maxima and V-row marks.

@@ -76,18 +76,12 @@ __device__ __forceinline__ void cp_async_lane(void* dst, const void* src) {
     else
         asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
-// 16 bytes, of which src_bytes (0 or 16) are read and the rest zero-filled.
-__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(src_bytes) : "memory");
-}
 // Arrive-on `bar` triggered when all of this thread's earlier cp.async copies
 // have completed; the barrier's expected count includes it (no increment).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }

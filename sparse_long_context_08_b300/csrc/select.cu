@@ -342,7 +342,7 @@ constexpr int kTkDigitBits = 11;
 constexpr int kTkBins = 1 << kTkDigitBits;
 constexpr int kTkMaxCluster = 8;
 
-struct TkShared {
+struct __align__(16) TkShared {
     int hist[2][kTkBins];            // one per radix pass, alternating (both zero between uses)
     int red[40];
     uint32_t umin[32], umax[32];
@@ -365,6 +365,11 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
+// The same with release semantics: this thread's earlier shared-memory writes
+// are visible to the cluster once the wait returns.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
@@ -374,6 +379,12 @@ __device__ __forceinline__ void st_cluster_u32(const void* p, uint32_t rank, uin
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+// 32-bit OR into the shared memory of CTA `rank` (no value returned).
+__device__ __forceinline__ void or_cluster_u32(const void* p, uint32_t rank, uint32_t v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+    asm volatile("red.shared::cluster.or.b32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
 // Block-wide min and max of one value per thread (every thread gets both).
@@ -429,9 +440,16 @@ __device__ void tk_boundary(const uint32_t (&key)[KPT], uint32_t valid, int n, i
                 atomicAdd(&hist[(key[j] >> shift) & dmask], 1);
         __syncthreads();
         if (wid == 0) {
-            int sum = 0;                                 // lane's bins [lane BPL, +BPL), rotated
-#pragma unroll 16
-            for (int i = 0; i < BPL; ++i) sum += hist[lane * BPL + ((i + lane) & (BPL - 1))];
+            // lane's bins [lane BPL, +BPL) as 16-byte loads, rotated by the lane
+            // (each quarter warp reads eight distinct bank groups)
+            const int4* h4 = reinterpret_cast<const int4*>(hist + lane * BPL);
+            int4 a4 = make_int4(0, 0, 0, 0);
+#pragma unroll 4
+            for (int i = 0; i < BPL / 4; ++i) {
+                const int4 v4 = h4[(i + lane) & (BPL / 4 - 1)];
+                a4.x += v4.x; a4.y += v4.y; a4.z += v4.z; a4.w += v4.w;
+            }
+            const int sum = (a4.x + a4.y) + (a4.z + a4.w);
             int incl = sum;                              // suffix sum over the lanes
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -524,12 +542,13 @@ __device__ __forceinline__ void tk_place(const uint32_t (&key)[KPT], uint32_t va
 // [C][slot] keys and pages.
 //
 // PG > 0 (csize = 1, PG = the group size): the selection also builds the
-// decode's union plan of each kv head (plan_from_rows) in the decode
+// decode's union plan of each kv head (plan_from_bits) in the decode
 // workspace `ws`.  Per-head selections run as a cluster of the group's PG
-// CTAs: each writes its row into the rank-0 CTA's shared memory, which builds
-// the plan; shared selections give every head the CTA's own row.  Dynamic
-// shared memory then also holds [PG][kp] rows, [PG][max_pages / 32] bitmap
-// words and [Umax] union pages.
+// CTAs: each ORs its pages into its bitmap in the rank-0 CTA's shared memory,
+// and the rank-0 CTA, which copied its sequence's page-table row into shared
+// memory at the start, builds the plan.  Shared selections set every head's
+// bitmap from the CTA's own row.  Dynamic shared memory then also holds
+// [PG][max_pages / 32] bitmap words and the [max_pages] page -> block map.
 template <int KPT, int PG>
 __global__ void __launch_bounds__(kTkThreads, 2)
 select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
@@ -537,7 +556,6 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
                        float* __restrict__ aux, int gs, int csize, WS ws, DecodeLayout L) {
     extern __shared__ __align__(16) int32_t s_row[];
     __shared__ TkShared sh;
-    __shared__ int s_cnt[8];
     const int tid = threadIdx.x;
     const int ng = gs > 0 ? gs : 1;
     const int unit = blockIdx.x / csize;
@@ -551,6 +569,29 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     const int p0 = (int)rank * chunk;
     const int span = max(0, min(kv.maxp - p0, chunk));
     const float* src = bound + (int64_t)bh * kv.maxp + p0;
+    // plan mode: the unit, this CTA's head within it (its cluster rank), and
+    // the rank-0 CTA's [PG][nwm] bitmaps and page -> block map (the sequence's
+    // page-table row, an input of the step rather than the previous kernel's
+    // output: copied in before the wait, checked where used)
+    const int pu = gs > 0 ? unit : bh / (PG > 0 ? PG : 1);
+    const uint32_t prank = (PG > 1 && gs == 0) ? cluster_rank() : 0u;
+    const int nwm = (kv.maxp + 31) / 32;
+    uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_row + kp);
+    int* s_pblk = reinterpret_cast<int*>(
+        (reinterpret_cast<uintptr_t>(s_bits + PG * nwm) + 15) & ~static_cast<uintptr_t>(15));
+    if constexpr (PG > 0) {
+        if (prank == 0) {
+            const int32_t* pt = kv.pt + (int64_t)b * kv.maxp;
+            const bool vec = (kv.maxp & 3) == 0 && (reinterpret_cast<uintptr_t>(kv.pt) & 15) == 0;
+            if (vec) {
+                for (int i = tid * 4; i < kv.maxp; i += kTkThreads * 4) cp_async16_zfill(s_pblk + i, pt + i, 16);
+            } else {
+                for (int i = tid; i < kv.maxp; i += kTkThreads) s_pblk[i] = __ldg(pt + i);
+            }
+            // cleared before the cluster barrier's arrive
+            for (int i = tid; i < PG * nwm; i += kTkThreads) s_bits[i] = 0u;
+        }
+    }
     pdl_wait();                         // the bounds are the previous kernel's output
     float v[KPT];
     {
@@ -580,23 +621,23 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     }
     const int np = min(kv.maxp, (kv.sl[b] + kv.P - 1) / kv.P);
     const int k = min(kp, np);
-    // plan mode: the unit, and this CTA's head within it (its cluster rank)
-    const int pu = gs > 0 ? unit : bh / (PG > 0 ? PG : 1);
-    const uint32_t prank = (PG > 1 && gs == 0) ? cluster_rank() : 0u;
+    if constexpr (PG > 0) {
+        if (prank == 0) plan_reset_unit(Hq, PG, ws, L, kv, pu);
+    }
     if (k <= 0) {                       // the same for every CTA of the cluster
         if (rank == 0 && tid < ng) {
             n_sel[bh + tid] = 0;
             if (aux) { aux[2 * (bh + tid)] = INFINITY; aux[2 * (bh + tid) + 1] = -INFINITY; }
         }
         if constexpr (PG > 0) {
-            if (prank == 0) {           // an empty plan
-                plan_reset_unit(Hq, PG, ws, L, kv, pu);
-                if (tid == 0) ws.union_count[pu] = 0;
-            }
+            if (prank == 0 && tid == 0) ws.union_count[pu] = 0;   // an empty plan
         }
         return;
     }
-    if (csize > 1 || (PG > 1 && gs == 0)) cluster_arrive_relaxed();   // waited for before the first remote store
+    // waited for before the first remote store (plan mode: the bitmaps were
+    // cleared before it)
+    if (PG > 1 && gs == 0) cluster_arrive_release();
+    else if (csize > 1) cluster_arrive_relaxed();
     const int n_loc = max(0, min(np - p0, chunk));
     for (int i = tid; i < 2 * kTkBins; i += kTkThreads) (&sh.hist[0][0])[i] = 0;
 
@@ -626,6 +667,27 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
                       [&](int j, int pos) { s_row[pos] = tid * KPT + j; }, tmin, nmax);
         // tk_place ends with a barrier: s_row is complete
         pdl_trigger();
+        if constexpr (PG > 0) {
+            if (gs > 0 || PG == 1) {
+                // one row for every head of the group
+                for (int r = tid; r < k; r += kTkThreads) {
+                    const int p = s_row[r];
+#pragma unroll
+                    for (int g = 0; g < PG; ++g) atomicOr(&s_bits[g * nwm + (p >> 5)], 1u << (p & 31));
+                }
+                cp_async_wait_all();    // this thread's part of the page -> block map
+                __syncthreads();
+            } else {
+                cluster_wait();         // every CTA of the cluster is running, bitmaps clear
+                // the row into this head's bitmap in the rank-0 CTA
+                for (int r = tid; r < k; r += kTkThreads) {
+                    const int p = s_row[r];
+                    or_cluster_u32(s_bits + prank * nwm + (p >> 5), 0u, 1u << (p & 31));
+                }
+                if (prank == 0) cp_async_wait_all();   // this thread's part of the map
+                cluster_sync_all();     // the bitmaps are in the rank-0 CTA, its map complete
+            }
+        }
         for (int x = tid; x < ng * k; x += kTkThreads) {
             const int g = x / k, r = x - g * k;
             sel[(int64_t)(bh + g) * kp + r] = s_row[r];
@@ -638,28 +700,8 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
             }
         }
         if constexpr (PG > 0) {
-            const int nwm = (kv.maxp + 31) / 32;
-            int* c_rows = s_row + kp;                                      // [PG][kp]
-            uint32_t* s_bits = reinterpret_cast<uint32_t*>(c_rows + PG * kp);
-            int* s_upage = reinterpret_cast<int*>(s_bits + PG * nwm);
-            if (gs > 0 || PG == 1) {
-                // one row for every head of the group
-                for (int x = tid; x < PG * k; x += kTkThreads) {
-                    const int g = x / k, r = x - g * k;
-                    c_rows[g * kp + r] = s_row[r];
-                }
-                if (tid < PG) s_cnt[tid] = k;
-            } else {
-                cluster_wait();         // every CTA of the cluster is running
-                for (int r = tid; r < k; r += kTkThreads)
-                    st_cluster_u32(c_rows + prank * kp + r, 0u, static_cast<uint32_t>(s_row[r]));
-                if (tid == 0) st_cluster_u32(&s_cnt[prank], 0u, static_cast<uint32_t>(k));
-                cluster_sync_all();     // the rows are in the rank-0 CTA
-                if (prank != 0) return; // nothing reads another CTA's memory past here
-            }
-            plan_reset_unit(Hq, PG, ws, L, kv, pu);
-            __syncthreads();
-            plan_from_rows<PG>(kv, kp, ws, L, pu, c_rows, s_cnt, s_bits, s_upage, sh.red);
+            // nothing reads another CTA's memory past the cluster barrier
+            if (prank == 0) plan_from_bits<PG>(kv, ws, L, pu, s_bits, nullptr, sh.red, s_pblk);
         }
         return;
     }
@@ -904,8 +946,9 @@ static cudaError_t launch_topk_reg(const float* bound, const KV& kv, int Hq, int
     const int slot = std::min(kp, chunk);
     if (csize > 1 && csize * slot > kTkThreads * KPT) return kShapeUnsupported;
     size_t smem = (size_t)kp * 4 + (csize > 1 ? (size_t)csize * slot * 8 : 0);
-    if (PG > 0)
-        smem += (size_t)PG * kp * 4 + (size_t)PG * ((kv.maxp + 31) / 32) * 4 + (size_t)L.Umax * 4;
+    if (PG > 0)   // [PG][nwm] bitmaps, [max_pages] page -> block (16-byte aligned)
+        smem = ((smem + (size_t)PG * ((kv.maxp + 31) / 32) * 4 + 15) & ~size_t(15)) +
+               (size_t)kv.maxp * 4;
     if (smem > 96 * 1024) return kShapeUnsupported;
     auto kernel = select_topk_reg_kernel<KPT, PG>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

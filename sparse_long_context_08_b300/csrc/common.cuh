@@ -331,6 +331,12 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, int
                  "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// The same with an L2 cache policy (createpolicy) for the read lines.
+__device__ __forceinline__ void cp_async16_zfill_hint(void* dst, const void* src, int src_bytes,
+                                                      uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes), "l"(policy) : "memory");
+}
 
 // L2 policy for data read once (the K/V pools and page metadata streams): the
 // lines are the first to go, so the small per-step arrays written between the

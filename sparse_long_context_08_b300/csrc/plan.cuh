@@ -65,14 +65,19 @@ __device__ void plan_from_bits(const KV& kv, const WS& ws, const DecodeLayout& L
     const int nwm = (kv.maxp + 31) / 32;
     const int b = u / kv.hkv;
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int nw = (pages_of(kv, b) + 31) / 32;
-    const int seg = (nw + nt - 1) / nt;
-    const int w0 = min(nw, tid * seg), w1 = min(nw, w0 + seg);
+    // bitmap bytes (8 pages each) split over the threads: a thread emits at
+    // most 8 pages per byte it holds
+    const int nb8 = (pages_of(kv, b) + 7) / 8;
+    const int seg = (nb8 + nt - 1) / nt;
+    const int y0 = min(nb8, tid * seg), y1 = min(nb8, y0 + seg);
+    auto head_byte = [&](int h, int y) -> uint32_t {
+        return (s_bits[h * nwm + (y >> 2)] >> (8 * (y & 3))) & 0xFFu;
+    };
     int cnt = 0;
-    for (int w = w0; w < w1; ++w) {
+    for (int y = y0; y < y1; ++y) {
         uint32_t x = 0;
 #pragma unroll
-        for (int h = 0; h < G; ++h) x |= s_bits[h * nwm + w];
+        for (int h = 0; h < G; ++h) x |= head_byte(h, y);
         cnt += __popc(x);
     }
     int total;
@@ -80,28 +85,29 @@ __device__ void plan_from_bits(const KV& kv, const WS& ws, const DecodeLayout& L
     int* upage = ws.union_page + (int64_t)u * L.Umax;
     int* umask = ws.union_mask + (int64_t)u * L.Umax;
     int* ublk = ws.union_blk + (int64_t)u * L.Umax;
-    for (int w = w0; w < w1; ++w) {
+    for (int y = y0; y < y1; ++y) {
         uint32_t hw[G];
         uint32_t uw = 0;
 #pragma unroll
-        for (int h = 0; h < G; ++h) { hw[h] = s_bits[h * nwm + w]; uw |= hw[h]; }
+        for (int h = 0; h < G; ++h) { hw[h] = head_byte(h, y); uw |= hw[h]; }
         while (uw) {
             const int bit = __ffs(uw) - 1;
             uw &= uw - 1;
             int mask = 0;
 #pragma unroll
             for (int h = 0; h < G; ++h) mask |= static_cast<int>((hw[h] >> bit) & 1u) << h;
-            upage[idx] = w * 32 + bit;
+            const int page = y * 8 + bit;
+            upage[idx] = page;
             umask[idx] = mask;
             if (s_pblk) {
-                int blk = s_pblk[w * 32 + bit];
+                int blk = s_pblk[page];
                 if (blk < 0 || blk >= kv.nb) {
                     flag_bad_data();
                     blk = -1;
                 }
                 ublk[idx] = blk;
             } else {
-                s_upage[idx] = w * 32 + bit;
+                s_upage[idx] = page;
             }
             ++idx;
         }

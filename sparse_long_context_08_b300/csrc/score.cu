@@ -448,6 +448,9 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
         static_assert(PPW >= 1 && PPT % kTcProdWarps == 0 && HKV % RPI == 0, "producer mapping");
         const int sub = lane / CPH, c = lane % CPH;
         const int kb = (c * 8) / 64, cin = c % 8;
+        // the metadata is read once: its lines go first, so the bounds this
+        // kernel writes are still in L2 for the selection
+        const uint64_t evict_first = l2_evict_first_policy();
         // this lane's page (warp * PPW + lane, lanes < PPW) of tile i: its page
         // table entry, checked only when used (the load stays in flight)
         constexpr int kNoPage = INT_MIN;               // lane without a page in the tile
@@ -501,7 +504,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
                 const int r = g * PPT + warp * PPW + pw;   // row within the tile
                 const bf16raw* src = msrc + ((int64_t)(blk >= 0 ? blk : 0) * HKV + g) * D + c * 8;
                 unsigned char* dst = st + kb * (kTcRows * 128) + r * 128 + ((cin ^ (r & 7)) * 16);
-                cp_async16_zfill(dst, src, blk >= 0 ? 16 : 0);
+                cp_async16_zfill_hint(dst, src, blk >= 0 ? 16 : 0, evict_first);
             }
             cp_async_arrive_noinc(&sh.full[s]);        // arrives once this thread's copies land
             // B for the tile's sequence, built while the copies are in flight

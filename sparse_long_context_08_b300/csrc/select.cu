@@ -497,8 +497,9 @@ __device__ void tk_boundary(const uint32_t (&key)[KPT], uint32_t valid, int n, i
 }
 
 // Output positions of this thread's taken keys (in key order) given the
-// boundary; calls f(j, pos) for each taken key j.  Also returns the smallest
-// taken and largest untaken valid key of the block (0 / 0 if none).
+// boundary; calls f(j, pos) for each taken key j, then a barrier.  Also
+// returns this thread's smallest taken and largest untaken valid key
+// (0xFFFFFFFF / 0 if none): tk_minmax of them gives the block's.
 template <int KPT, typename F>
 __device__ __forceinline__ void tk_place(const uint32_t (&key)[KPT], uint32_t valid, int shift,
                                          uint64_t hi, int takeB, TkShared& sh, F&& f,
@@ -530,7 +531,7 @@ __device__ __forceinline__ void tk_place(const uint32_t (&key)[KPT], uint32_t va
             }
             if (take) mn = min(mn, key[j]); else mx = max(mx, key[j]);
         }
-    tk_minmax(mn, mx, sh);
+    __syncthreads();
     tmin = mn;
     nmax = mx;
 }
@@ -630,7 +631,10 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
             if (aux) { aux[2 * (bh + tid)] = INFINITY; aux[2 * (bh + tid) + 1] = -INFINITY; }
         }
         if constexpr (PG > 0) {
-            if (prank == 0 && tid == 0) ws.union_count[pu] = 0;   // an empty plan
+            if (prank == 0) {
+                if (tid == 0) ws.union_count[pu] = 0;             // an empty plan
+                cp_async_wait_all();    // no copy into shared memory outlives the CTA
+            }
         }
         return;
     }
@@ -692,16 +696,17 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
             const int g = x / k, r = x - g * k;
             sel[(int64_t)(bh + g) * kp + r] = s_row[r];
         }
-        if (tid < ng) {
-            n_sel[bh + tid] = k;
-            if (aux) {
-                aux[2 * (bh + tid)] = key_float(tmin);
-                aux[2 * (bh + tid) + 1] = k < np ? key_float(nmax) : -INFINITY;
-            }
-        }
+        if (tid < ng) n_sel[bh + tid] = k;
         if constexpr (PG > 0) {
             // nothing reads another CTA's memory past the cluster barrier
             if (prank == 0) plan_from_bits<PG>(kv, ws, L, pu, s_bits, nullptr, sh.red, s_pblk);
+        }
+        if (aux) {                      // off the critical path: the boundary keys
+            tk_minmax(tmin, nmax, sh);
+            if (tid < ng) {
+                aux[2 * (bh + tid)] = key_float(tmin);
+                aux[2 * (bh + tid) + 1] = k < np ? key_float(nmax) : -INFINITY;
+            }
         }
         return;
     }
@@ -719,6 +724,7 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
                           st_cluster_u32(c_page + rank * slot + pos, 0u,
                                          static_cast<uint32_t>(p0 + tid * KPT + j));
                       }, tmin, nmax);
+        tk_minmax(tmin, nmax, sh);
     } else {
         nmax = 0u;
     }
@@ -753,6 +759,7 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
     tk_boundary<KPT>(ck, cvalid, m, k, kmn, kmx, sh, shift, hi, takeB);
     tk_place<KPT>(ck, cvalid, shift, hi, takeB, sh,
                   [&](int j, int pos) { s_row[pos] = c_page[tid * KPT + j]; }, tmin, nmax);
+    tk_minmax(tmin, nmax, sh);
     for (int x = tid; x < ng * k; x += kTkThreads) {
         const int g = x / k, r = x - g * k;
         sel[(int64_t)(bh + g) * kp + r] = s_row[r];

@@ -338,6 +338,12 @@ __device__ __forceinline__ void cp_async16_zfill_hint(void* dst, const void* src
                  ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes), "l"(policy) : "memory");
 }
 
+// Requests the 128-byte line holding p into L2 (and its address translation);
+// no value is read, so the line may still be written by another kernel.
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // L2 policy for data read once (the K/V pools and page metadata streams): the
 // lines are the first to go, so the small per-step arrays written between the
 // kernels (bounds, scores) stay in L2 for the next kernel.

@@ -444,6 +444,7 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
     unsigned char* ring = s_qm + (size_t)warp * ns * page_bytes;
     int* s_prefix = reinterpret_cast<int*>(s_qm + (size_t)kQmWarps * ns * page_bytes);
     uint64_t* bar = s_bar[warp];
+    for (int i = tid * 32; i < L.U; i += blockDim.x * 32) prefetch_l2_line(ws.union_count + i);
     pdl_wait();                 // the union plan is the previous kernel's output
     {
         const int U = L.U;
@@ -913,6 +914,8 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
     float* outb = out + (int64_t)bh * D;
 
     // 1. the union size and the head's per-page maxima
+    for (int i = tid * 32; i < L.Umax; i += kTpvThreads * 32) prefetch_l2_line(pmr + i);
+    if (tid == 0) prefetch_l2_line(ws.union_count + u);
     pdl_wait();                               // the scores are the previous kernel's output
     const int ucnt = __ldcg(ws.union_count + u);
     float pm[kTpvPmVec];

@@ -593,6 +593,16 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
             for (int i = tid; i < PG * nwm; i += kTkThreads) s_bits[i] = 0u;
         }
     }
+    // the bound rows are still being written: only their lines' translation
+    // and L2 placement are requested; the sequence length is an input
+    {
+        const int lines = (span + 31) / 32;
+        for (int x = tid; x < ng * lines; x += kTkThreads) {
+            const int g = x / lines;
+            prefetch_l2_line(src + (int64_t)g * kv.maxp + (x - g * lines) * 32);
+        }
+    }
+    const int seq_len = __ldg(kv.sl + b);
     pdl_wait();                         // the bounds are the previous kernel's output
     float v[KPT];
     {
@@ -620,7 +630,7 @@ select_topk_reg_kernel(const float* __restrict__ bound, KV kv, int Hq, int kp,
             }
         }
     }
-    const int np = min(kv.maxp, (kv.sl[b] + kv.P - 1) / kv.P);
+    const int np = min(kv.maxp, (seq_len + kv.P - 1) / kv.P);
     const int k = min(kp, np);
     if constexpr (PG > 0) {
         if (prank == 0) plan_reset_unit(Hq, PG, ws, L, kv, pu);

@@ -102,6 +102,8 @@ plan_kernel(KV kv, int Hq, const int32_t* __restrict__ sel, const int32_t* __res
     __shared__ int s_ns[G];
     const int nwm = (kv.maxp + 31) / 32;
     int* s_upage = reinterpret_cast<int*>(s_plan + (size_t)G * nwm);
+    pdl_wait();                         // the selection is the previous kernel's output
+    pdl_trigger();                      // the q.K kernel's CTAs may take their places
     build_plan<G>(kv, Hq, sel, n_sel, cap, ws, L, blockIdx.x, s_plan, s_upage, s_upage + L.Umax,
                   red, s_ns);
 }
@@ -628,6 +630,7 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
 // tpv: exact alpha-entmax threshold and value accumulation, one CTA per head
 // ---------------------------------------------------------------------------
 constexpr int kTpvPmVec = 8;          // page maxima per thread per round trip
+constexpr int kTpvPruneTokens = 2048;  // candidate pages' tokens above which t is first bounded
 
 // Union pages i < ucnt of a head whose largest z' exceeds max - 1 (only those
 // can hold a token with nonzero weight), written to list[] in a fixed thread
@@ -693,9 +696,40 @@ __device__ __forceinline__ bool threshold_step(float f, float d, float h, float&
 
 // The threshold t of the m candidates x (relative to the max; e = 1, 2) by
 // threshold_step, every thread of the block taking part.
+// The same by one warp for m <= 1024 candidates (32 per lane in registers,
+// shuffle-only reductions), from the bracket [t0, 0] (f(t0) >= 0).
+template <int E>
+__device__ float warp_threshold(const float* s_vals, int m, float t0) {
+    const int lane = threadIdx.x & 31;
+    float xr[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int i = j * 32 + lane;
+        xr[j] = i < m ? s_vals[i] : -INFINITY;
+    }
+    float tt = t0, lo = t0, hi = 0.f;
+    for (int it = 0; it < 64; ++it) {
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float a = xr[j] - tt;
+            if (a > 0.f) {
+                if (E == 2) { s0 = fmaf(a, a, s0); s1 += a; s2 += 1.f; }
+                else { s0 += a; s1 += 1.f; }
+            }
+        }
+        s0 = warp_sum(s0);
+        s1 = warp_sum(s1);
+        if (E == 2) s2 = warp_sum(s2);
+        if (threshold_step(s0 - 1.f, E == 2 ? 2.f * s1 : s1, E == 2 ? 2.f * s2 : 0.f, tt, lo, hi))
+            break;
+    }
+    return tt;
+}
+
 template <int E, bool kGlobal>
-__device__ float solve_threshold(const float* x, int m, float4* red) {
-    float t = -1.f, lo = -1.f, hi = 0.f;
+__device__ float solve_threshold(const float* x, int m, float4* red, float t0 = -1.f) {
+    float t = t0, lo = t0, hi = 0.f;
     for (int it = 0; it < 64; ++it) {
         float3 acc = make_float3(0.f, 0.f, 0.f);
         for (int i = threadIdx.x; i < m; i += blockDim.x) {
@@ -942,10 +976,46 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
         }
         return;
     }
-    const int npl = list_candidate_pages(pm, pmr, ucnt, mx, s_pl, ired);   // ends with a barrier
+    int npl = list_candidate_pages(pm, pmr, ucnt, mx, s_pl, ired);   // ends with a barrier
+
+    // 1b. many candidate tokens: a lower bound of t from the candidate pages'
+    // maxima (scores of tokens of the head): their own threshold t_S solves
+    // f_S(t_S) = 0 with f_S <= f, so t_S <= t.  Pages whose maximum is at most
+    // t_S hold no token of the support and are dropped, tokens at or below it
+    // are not candidates, and the solve below starts from t_S.
+    float tlo = -1.f;
+    if (E != 0 && (npl << pshift) > kTpvPruneTokens && npl <= cand_cap) {
+        for (int k = tid; k < npl; k += kTpvThreads) s_x[k] = __ldcg(pmr + s_pl[k]) - mx;
+        __syncthreads();
+        float ts;
+        if (npl <= 1024) {
+            if (wid == 0) {
+                const float tt = warp_threshold<E>(s_x, npl, -1.f);
+                if (lane == 0) s_t = tt;
+            }
+            __syncthreads();
+            ts = s_t;
+        } else {
+            ts = solve_threshold<E, false>(s_x, npl, f4red);
+        }
+        tlo = ts - 1e-6f;                     // a margin for the rounding of t_S
+        int nl = 0;                           // kept pages, in order, through s_pb
+        for (int base = 0; base < npl; base += kTpvThreads) {
+            const int k = base + tid;
+            const bool keep = k < npl && s_x[k] > tlo;
+            int tot;
+            const int pos = nl + block_exclusive_scan(keep ? 1 : 0, ired, &tot);
+            if (keep) s_pb[pos] = s_pl[k];
+            nl += tot;
+        }
+        __syncthreads();
+        for (int k = tid; k < nl; k += kTpvThreads) s_pl[k] = s_pb[k];
+        npl = nl;
+        __syncthreads();
+    }
 
     // 2. the candidate pages' scores and blocks (all loads in flight before any
-    // is used); candidates x = z' - max > -1 in a fixed thread order, pos =
+    // is used); candidates x = z' - max > tlo in a fixed thread order, pos =
     // index into the candidate pages' tokens
     const int ne = npl << pshift;
     const int* ublk = ws.union_blk + (int64_t)u * L.Umax;
@@ -966,12 +1036,12 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
         for (int j = 0; j < kTpvVec * 4; ++j) v[j] -= mx;
         int c = 0;
 #pragma unroll
-        for (int j = 0; j < kTpvVec * 4; ++j) c += v[j] > -1.f;
+        for (int j = 0; j < kTpvVec * 4; ++j) c += v[j] > tlo;
         int tot;
         int pos = m + block_exclusive_scan(c, ired, &tot);
 #pragma unroll
         for (int j = 0; j < kTpvVec * 4; ++j) {
-            if (v[j] > -1.f) {
+            if (v[j] > tlo) {
                 if (pos < cand_cap) {
                     s_x[pos] = v[j];
                     s_pos[pos] = t0 + j * kTpvThreads + tid;
@@ -987,38 +1057,14 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
     // 3. threshold t (relative to the max): f(t) = sum (x - t)_+^e - 1 = 0
     float t;
     if (E != 0 && m <= 1024) {
-        // one warp, candidates in registers, shuffle-only reductions
         if (wid == 0) {
-            float xr[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int i = j * 32 + lane;
-                xr[j] = i < m ? s_x[i] : -INFINITY;
-            }
-            float tt = -1.f, lo = -1.f, hi = 0.f;
-            for (int it = 0; it < 64; ++it) {
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float a = xr[j] - tt;
-                    if (a > 0.f) {
-                        if (E == 2) { s0 = fmaf(a, a, s0); s1 += a; s2 += 1.f; }
-                        else { s0 += a; s1 += 1.f; }
-                    }
-                }
-                s0 = warp_sum(s0);
-                s1 = warp_sum(s1);
-                if (E == 2) s2 = warp_sum(s2);
-                if (threshold_step(s0 - 1.f, E == 2 ? 2.f * s1 : s1, E == 2 ? 2.f * s2 : 0.f, tt,
-                                   lo, hi))
-                    break;
-            }
+            const float tt = warp_threshold<E>(s_x, m, tlo);
             if (lane == 0) s_t = tt;
         }
         __syncthreads();
         t = s_t;
     } else if (E != 0) {
-        t = solve_threshold<E, false>(s_x, m, f4red);
+        t = solve_threshold<E, false>(s_x, m, f4red, tlo);
     } else {
         const float ex = 1.f / (alpha - 1.f);
         float lo = -1.f, hi = -powf(static_cast<float>(m), 1.f - alpha);
@@ -1683,7 +1729,7 @@ static cudaError_t launch_decode_t(const float* q, int Hq, float scale, const KV
         e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
-        e = launch_kernel(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel,
+        e = launch_kernel_pdl(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel,
                           n_sel, cap, ws, L);
         if (e != cudaSuccess) return e;
     }
@@ -1735,7 +1781,7 @@ static cudaError_t launch_decode_softmax_t(const float* q, int Hq, float scale, 
         const size_t smem = plan_smem_bytes(G, kv.maxp, L.Umax, cap);
         e = cudaFuncSetAttribute(plan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        e = launch_kernel(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel,
+        e = launch_kernel_pdl(plan_kernel<G>, dim3(L.U), dim3(kPlanThreads), smem, s, kv, Hq, sel, n_sel,
                           cap, ws, L);
     }
     if (e != cudaSuccess) return e;

@@ -248,6 +248,7 @@ score_kernel(const float* __restrict__ q, int Hq, float scale, KV kv,
         }
         cp_async_wait<0>();
     }
+    pdl_trigger();                      // the selection's CTAs may take their places
 }
 
 // ---------------------------------------------------------------------------

@@ -849,6 +849,7 @@ select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float 
     const int np = min(kv.maxp, (len + kv.P - 1) / kv.P);
     const float c = alpha - 1.f;
     const float* src = ms + (int64_t)bh * kv.maxp * 2;
+    pdl_wait();                         // the page scores are the previous kernel's output
     float mu_max = -INFINITY;
     for (int p = threadIdx.x; p < np; p += blockDim.x) {
         const float m = src[2 * p], s = src[2 * p + 1];
@@ -913,6 +914,7 @@ select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float 
         }
     }
     const float tau_hat = tau;
+    pdl_trigger();                      // the decode's CTAs may take their places
 
     // threshold test; the uint32 key of a page that fails is 0 (below all)
     int pass = 0;
@@ -1065,14 +1067,14 @@ cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, 
         e = cudaFuncSetAttribute(select_gauss_kernel<2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        e = launch_kernel(select_gauss_kernel<2>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
+        e = launch_kernel_pdl(select_gauss_kernel<2>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
                           Hq, cap, alpha, delta, sel, n_sel, aux);
         if (e != cudaSuccess) return e;
     } else {
         e = cudaFuncSetAttribute(select_gauss_kernel<1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        e = launch_kernel(select_gauss_kernel<1>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
+        e = launch_kernel_pdl(select_gauss_kernel<1>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
                           Hq, cap, alpha, delta, sel, n_sel, aux);
         if (e != cudaSuccess) return e;
     }

@@ -809,39 +809,39 @@ __device__ __forceinline__ float2 normal_cdf_pdf(float u) {
 // Also returns the second derivative d2E/dtau^2 (z): e = 2: 2 Phi(u);
 // e = 1: phi(u) / sig (sig = 0: 2 [a > 0] and 0, the kinks aside).
 template <int E>
-__device__ __forceinline__ float3 gauss_moment(float mu, float sig, float tau) {
+__device__ __forceinline__ float3 gauss_moment(float mu, float sig, float isig, float tau) {
     const float a = mu - tau;
     if (!(sig > 0.f)) {
         const float ap = fmaxf(a, 0.f);
         return E == 2 ? make_float3(ap * ap, 2.f * ap, a > 0.f ? 2.f : 0.f)
                       : make_float3(ap, a > 0.f ? 1.f : 0.f, 0.f);
     }
-    const float u = a / sig;
+    const float u = a * isig;
     const float2 cp = normal_cdf_pdf(u);
     const float Phi = cp.x, phi = cp.y;
     const float m1 = fmaf(a, Phi, sig * phi);
     if (E == 2)
         return make_float3(fmaf(fmaf(a, a, sig * sig), Phi, a * sig * phi), 2.f * m1, 2.f * Phi);
-    return make_float3(m1, Phi, phi / sig);
+    return make_float3(m1, Phi, phi * isig);
 }
 
-template <int E>
+template <int E, int KPT>
 __global__ void __launch_bounds__(kSelThreads, 2)
 select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float alpha,
                     float delta, int32_t* __restrict__ sel, int32_t* __restrict__ n_sel,
                     float* __restrict__ aux) {
+    // shared layout: the top-k scratch (TkShared), then per page: scaled mean,
+    // scaled std, its reciprocal, key
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ SelShared sh;
     __shared__ float4 fred[32];
     __shared__ float fmaxred[32];
-    const int nw = blockDim.x >> 5;
-    int* whist = reinterpret_cast<int*>(smem_raw);
-    int* hist = whist + nw * 256;
+    TkShared& tsh = *reinterpret_cast<TkShared*>(smem_raw);
     const int np_max = kv.maxp;
-    float* s_mu = reinterpret_cast<float*>(hist + 256);
+    float* s_mu = reinterpret_cast<float*>(smem_raw + sizeof(TkShared));
     float* s_sg = s_mu + np_max;
-    float* s_n = s_sg + np_max;
-    uint32_t* keys = reinterpret_cast<uint32_t*>(s_n + np_max);
+    float* s_isg = s_sg + np_max;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(s_isg + np_max);
 
     const int bh = blockIdx.x;
     const int b = bh / Hq;
@@ -857,7 +857,7 @@ select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float 
         const float zmax = n > 1 ? fmaf(sqrtf(2.f * logf(static_cast<float>(n))), s, m) : m;
         s_mu[p] = c * m;
         s_sg[p] = c * s;
-        s_n[p] = static_cast<float>(n);
+        s_isg[p] = c * s > 0.f ? 1.f / (c * s) : 0.f;
         keys[p] = float_key(zmax);
         mu_max = fmaxf(mu_max, c * m);
     }
@@ -880,10 +880,11 @@ select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float 
     for (int it = 0; it < 64; ++it) {
         float3 acc = make_float3(0.f, 0.f, 0.f);
         for (int p = threadIdx.x; p < np; p += blockDim.x) {
-            const float3 v = gauss_moment<E>(s_mu[p], s_sg[p], tau);
-            acc.x = fmaf(s_n[p], v.x, acc.x);
-            acc.y = fmaf(s_n[p], v.y, acc.y);
-            acc.z = fmaf(s_n[p], v.z, acc.z);
+            const float3 v = gauss_moment<E>(s_mu[p], s_sg[p], s_isg[p], tau);
+            const float n = static_cast<float>(min(kv.P, len - p * kv.P));   // tokens of the page
+            acc.x = fmaf(n, v.x, acc.x);
+            acc.y = fmaf(n, v.y, acc.y);
+            acc.z = fmaf(n, v.z, acc.z);
         }
         acc = block_sum3(acc, fred);
         const float F = acc.x - 1.f, dF = acc.y, H = acc.z;
@@ -925,24 +926,43 @@ select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float 
         if (!ok) keys[p] = 0u;
     }
     pass = block_sum_i(pass, sh.red);
-    int32_t* dst = sel + (int64_t)bh * cap;
-    uint32_t kth = 1u;   // every passing page has a key >= 1
-    int take_eq = 0;
-    if (pass > cap) {
-        radix_kth(keys, np, cap, whist, hist, sh, kth, take_eq);
-    } else if (pass == 0) {
+    if (pass == 0) {
         // no page clears the threshold: keep the argmax estimated max (lowest id)
         for (int p = threadIdx.x; p < np; p += blockDim.x) {
             const int n = min(kv.P, len - p * kv.P);
             const float m = src[2 * p], s = src[2 * p + 1];
             keys[p] = float_key(n > 1 ? fmaf(sqrtf(2.f * logf(static_cast<float>(n))), s, m) : m);
         }
-        radix_kth(keys, np, 1, whist, hist, sh, kth, take_eq);
     }
-    uint32_t next_key;
-    const int got = compact_topk(keys, np, kth, take_eq, dst, sh, &next_key);
+    // the k largest keys (failing pages hold 0, below every passing key), in
+    // page order, with the register-resident radix boundary of the top-k
+    // selection: pages [tid KPT, (tid + 1) KPT) per thread
+    const int k = pass > cap ? cap : (pass == 0 ? 1 : pass);
+    for (int i = threadIdx.x; i < 2 * kTkBins; i += blockDim.x) (&tsh.hist[0][0])[i] = 0;
+    __syncthreads();
+    uint32_t key[KPT];
+    uint32_t valid = 0u;
+    uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int p = threadIdx.x * KPT + j;
+        key[j] = p < np ? keys[p] : 0u;
+        if (p < np) {
+            valid |= 1u << j;
+            kmn = min(kmn, key[j]);
+            kmx = max(kmx, key[j]);
+        }
+    }
+    tk_minmax(kmn, kmx, tsh);
+    int shift, takeB;
+    uint64_t bhi;
+    uint32_t tmin, nmax;
+    tk_boundary<KPT>(key, valid, np, k, kmn, kmx, tsh, shift, bhi, takeB);
+    int32_t* dst = sel + (int64_t)bh * cap;
+    tk_place<KPT>(key, valid, shift, bhi, takeB, tsh,
+                  [&](int j, int pos) { dst[pos] = threadIdx.x * KPT + j; }, tmin, nmax);
     if (threadIdx.x == 0) {
-        n_sel[bh] = got;
+        n_sel[bh] = k;
         if (aux) { aux[2 * bh] = tau_hat; aux[2 * bh + 1] = static_cast<float>(pass); }
     }
 }
@@ -1055,30 +1075,31 @@ cudaError_t launch_select_topk(const float* bound, const KV& kv, int Hq, int kp,
                          kp, sel, n_sel, aux, gs);
 }
 
+template <int E, int KPT>
+static cudaError_t launch_gauss_t(const float* ms, const KV& kv, int Hq, int cap, float alpha,
+                                  float delta, int32_t* sel, int32_t* n_sel, float* aux, size_t smem,
+                                  cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(select_gauss_kernel<E, KPT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel_pdl(select_gauss_kernel<E, KPT>, dim3(kv.B * Hq), dim3(kSelThreads), smem,
+                             s, ms, kv, Hq, cap, alpha, delta, sel, n_sel, aux);
+}
+
 cudaError_t launch_select_gauss(const float* ms, const KV& kv, int Hq, int cap, float alpha,
                                 float delta, int32_t* sel, int32_t* n_sel, float* aux,
                                 cudaStream_t s) {
-    const int threads = kSelThreads;
-    const size_t smem = (size_t)(threads / 32) * 256 * 4 + 256 * 4 + (size_t)kv.maxp * 16;
-    if ((int)smem > max_optin_smem() - 1024) return kShapeUnsupported;
+    const size_t smem = sizeof(TkShared) + (size_t)kv.maxp * 16;
+    if ((int)smem > max_optin_smem() - 1024 || kv.maxp > kSelThreads * 24) return kShapeUnsupported;
     const bool e2 = fabsf(alpha - 1.5f) < 1e-6f;
-    cudaError_t e;
-    if (e2) {
-        e = cudaFuncSetAttribute(select_gauss_kernel<2>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = launch_kernel_pdl(select_gauss_kernel<2>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
-                          Hq, cap, alpha, delta, sel, n_sel, aux);
-        if (e != cudaSuccess) return e;
-    } else {
-        e = cudaFuncSetAttribute(select_gauss_kernel<1>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = launch_kernel_pdl(select_gauss_kernel<1>, dim3(kv.B * Hq), dim3(threads), smem, s, ms, kv,
-                          Hq, cap, alpha, delta, sel, n_sel, aux);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaGetLastError();
+    if (kv.maxp <= kSelThreads * 8)
+        return e2 ? launch_gauss_t<2, 8>(ms, kv, Hq, cap, alpha, delta, sel, n_sel, aux, smem, s)
+                  : launch_gauss_t<1, 8>(ms, kv, Hq, cap, alpha, delta, sel, n_sel, aux, smem, s);
+    if (kv.maxp <= kSelThreads * 16)
+        return e2 ? launch_gauss_t<2, 16>(ms, kv, Hq, cap, alpha, delta, sel, n_sel, aux, smem, s)
+                  : launch_gauss_t<1, 16>(ms, kv, Hq, cap, alpha, delta, sel, n_sel, aux, smem, s);
+    return e2 ? launch_gauss_t<2, 24>(ms, kv, Hq, cap, alpha, delta, sel, n_sel, aux, smem, s)
+              : launch_gauss_t<1, 24>(ms, kv, Hq, cap, alpha, delta, sel, n_sel, aux, smem, s);
 }
 
 }  // namespace ekv

@@ -72,6 +72,9 @@ def parse():
                          "softmax; meta: the page-metadata build (prefill) alone")
     ap.add_argument("--cpu-1core", action="store_true",
                     help="also time the oracle on one host thread (cpu_baseline_1core)")
+    ap.add_argument("--e2e-breakdown", action="store_true",
+                    help="where the end-to-end step time goes: host wall clock of a tiny graph, "
+                         "the device-only step graph and the host-buffer step, each with its sync")
     return ap.parse_args()
 
 
@@ -127,6 +130,18 @@ def measured_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (the oracle baseline's hardware)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 def workload_config(w):
@@ -388,7 +403,8 @@ def run_reference(args):
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": dict(workload_config(w), mode=args.mode),
                 "cpu_baseline": {"value": us, "unit": "us/step", "cores": cores,
-                                 "kind": "oracle", "sample": desc},
+                                 "kind": "oracle", "sample": desc,
+               "cpu_model": host_cpu_model()},
                 "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0},
                 "gpu_launches": 0}
@@ -545,14 +561,16 @@ def run_ours(args):
         e2e = {"value": whole_job_us_per_step(max_over_ranks(sum(times), world, "cuda") * 1e3 / K,
                                               world), "unit": "us/step",
                "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4,
-               "timing": "host wall clock per step: step_host (one graph replay of the pinned "
-                         "H2D of q, the step's kernels and the D2H of out) and the sync"}
+               "timing": "host wall clock per step: step_host (one graph replay: a kernel "
+                         "copying q from pinned host memory, the step's kernels, the last "
+                         "writing out into pinned host memory) and the sync"}
 
     cpu = None
     ties = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, desc, cores, _ = oracle_time_per_step(w, args.cpu_seconds)
-        cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc,
+               "cpu_model": host_cpu_model()}
         import numpy as np
         BH = w.batch * w.num_q_heads
         sample = np.sort(np.random.default_rng(5).choice(BH, size=min(BH, 32), replace=False))
@@ -737,7 +755,8 @@ def run_full(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, desc, cores = oracle_full_time_per_step(w, args.cpu_seconds, mode=mode)
-        cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc,
+               "cpu_model": host_cpu_model()}
 
     if world > 1:
         dist.barrier()
@@ -848,8 +867,76 @@ def run_meta(args):
         dist.destroy_process_group()
 
 
+def run_e2e_breakdown(args):
+    """Host wall clock (median of 200, the GPU idle before each call) of the
+    pieces of an end-to-end step: a graph of one tiny kernel plus the stream
+    sync (the launch and wake-up floor), the device-only step graph plus the
+    sync, and the host-buffer step (EntmaxKVDecoder.step_host) plus the sync.
+    One JSON line."""
+    import torch
+
+    from sparse_long_context_08_b300.api import EntmaxKVDecoder, upload_workload
+    from sparse_long_context_08_b300.workloads import make_workload
+
+    w = make_workload(args.workload, **overrides(args))
+    kv, q = upload_workload(w)
+    dec = EntmaxKVDecoder(kv, w.num_q_heads, float(w.scale), w.alpha, w.policy,
+                          w.budget_tokens, w.delta)
+    dec.build_meta()
+    torch.cuda.synchronize()
+    flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    q_host = q.cpu().pin_memory()
+    out_host = torch.empty(dec.out.shape, dtype=torch.float32).pin_memory()
+    q_dev = torch.empty_like(q)
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            dec.step(q)
+    s.synchronize()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=s):
+        dec.step(q)
+    tiny = torch.zeros(1, device="cuda")
+    with torch.cuda.stream(s):
+        tiny.add_(1)
+    g_tiny = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_tiny, stream=s):
+        tiny.add_(1)
+    for _ in range(3):
+        dec.step_host(q_host, out_host, q_dev, s)
+        s.synchronize()
+
+    def replay(g):
+        def f():
+            with torch.cuda.stream(s):
+                g.replay()
+        return f
+
+    def median_us(fn, n=200):
+        ts = []
+        for i in range(n):
+            flush.fill_(i & 255)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            s.synchronize()
+            ts.append((time.perf_counter() - t0) * 1e6)
+        return statistics.median(ts)
+
+    rows = {"tiny_graph_and_sync_us": median_us(replay(g_tiny)),
+            "device_step_graph_and_sync_us": median_us(replay(g_step)),
+            "step_host_and_sync_us": median_us(
+                lambda: dec.step_host(q_host, out_host, q_dev, s))}
+    print(json.dumps({"e2e_breakdown": rows, "workload": workload_config(w)["workload"],
+                      "timing": "host wall clock, median of 200 calls, L2 flushed and the GPU "
+                                "idle before each"}), flush=True)
+
+
 def main():
     args = parse()
+    if args.e2e_breakdown:
+        run_e2e_breakdown(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     elif args.mode == "meta":

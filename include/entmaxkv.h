@@ -151,10 +151,13 @@ int entmaxkv_select(const float* page_scores, const ekv_paged_kv* kv,
  * For each (b, h): the valid tokens of pages sel[b, h, 0:n_sel[b, h]] (distinct
  * ids, any order, each < ceil(seq_lens[b] / page_size); duplicates count once)
  * are scored z = scale q.k, tau is the exact alpha-entmax threshold of
- * (alpha-1) z over them (Newton from the left for alpha 1.5 and 2, bisection
- * otherwise), and out = sum_i p_i v_i / sum_i p_i.  Each kv head's K page is
- * read once per step for its whole query group; only the V rows of tokens with
- * p_i > 0 are read.
+ * (alpha-1) z over them (a safeguarded Halley iteration for alpha 1.5 and 2,
+ * bisection otherwise), and out = sum_i p_i v_i / sum_i p_i.  Each kv head's K
+ * page is read once per step for its whole query group; only the V rows of
+ * tokens with p_i > 0 are read.
+ * out fp32 [batch, num_q_heads, head_dim]: device memory, or pinned host memory
+ * mapped into the device's address space (the kernel then writes the result
+ * there directly); any other pointer is EKV_INVALID_ARG.
  * tau_out (nullable) fp32 [batch, num_q_heads] in (alpha-1) z units; support_out
  * (nullable) int32 [batch, num_q_heads] = #{p_i > 0}.  An empty selection gives
  * out = 0, tau = +inf, support 0.  alpha > 1.  workspace: device scratch of at
@@ -300,6 +303,17 @@ int entmaxkv_read_device_status(int32_t* status_out /* host */, void* stream);
  * reports EKV_DEVICE_TIMEOUT.  No memory is copied and nothing waits on the
  * kernel.  Returns EKV_INVALID_ARG for a limit outside the range. */
 int entmaxkv_check_wait_timeout(uint32_t limit_us, void* stream);
+
+/* Input staging for a step whose query is in pinned host memory (not part of
+ * the method): copies `bytes` from src to dst on `stream` with a kernel rather
+ * than a copy engine, so a captured step has no copy-engine hand-off before its
+ * first kernel; the score kernel that follows sets up while the copy runs and
+ * reads q only after it.  src and dst must be device-accessible: device memory,
+ * or host memory mapped into the device's address space (pinned, unified
+ * addressing).  Returns EKV_INVALID_ARG for a null or inaccessible pointer;
+ * bytes = 0 does nothing.  The caller keeps both buffers alive until the copy
+ * has run. */
+int entmaxkv_copy_in(void* dst, const void* src, size_t bytes, void* stream);
 
 /* Measurement aid (not part of the method): record four caller-created
  * cudaEvent_t handles around the kernels of every later entmaxkv_decode call on

@@ -111,14 +111,17 @@ class EntmaxKVDecoder(_HostStepGraphs):
                           self.alpha, self.out, self.tau, self.support, self.workspace, stream)
         return self.out
 
-    def select_decode(self, q: torch.Tensor, stream=None) -> torch.Tensor:
+    def select_decode(self, q: torch.Tensor, stream=None, out: torch.Tensor | None = None):
         """select then decode in one library call (the selection also builds
-        the decode's page union); the same results as select() and decode()."""
+        the decode's page union); the same results as select() and decode().
+        out: where the result goes (default self.out; pinned host memory is
+        written by the kernel directly)."""
+        out = self.out if out is None else out
         E.entmaxkv_select_decode(self.page_scores, q, self.Hq, self.scale, self.kv, self.policy,
                                  self.budget, self.alpha, self.delta, self.sel, self.n_sel,
-                                 self.aux, self.out, self.tau, self.support, self.workspace,
+                                 self.aux, out, self.tau, self.support, self.workspace,
                                  stream)
-        return self.out
+        return out
 
     def step(self, q: torch.Tensor, stream=None) -> torch.Tensor:
         """One decode step for device-resident q [B, Hq, d]; returns `out` (device)."""
@@ -127,15 +130,17 @@ class EntmaxKVDecoder(_HostStepGraphs):
 
     def _step_host_eager(self, q_host, out_host, q_dev, s) -> None:
         with torch.cuda.stream(s):
-            q_dev.copy_(q_host, non_blocking=True)
-            self.step(q_dev, s)
-            out_host.copy_(self.out, non_blocking=True)
+            E.entmaxkv_copy_in(q_dev, q_host, s)      # a kernel, no copy-engine hand-off
+            self.score(q_dev, s)
+            self.select_decode(q_dev, s, out=out_host)   # the result written to host memory
 
     def step_host(self, q_host: torch.Tensor, out_host: torch.Tensor, q_dev: torch.Tensor,
                   stream=None) -> None:
-        """One decode step from host memory: q_host (pinned) -> device, the three
-        stages, then out -> out_host (pinned).  Asynchronous on `stream`; replayed
-        as one CUDA graph per set of buffers (see _HostStepGraphs)."""
+        """One decode step from host memory: q_host (pinned) -> q_dev by a
+        copy kernel, the stages, and the result written by the last kernel
+        straight into out_host (pinned); self.out is not written.
+        Asynchronous on `stream`; replayed as one CUDA graph per set of
+        buffers (see _HostStepGraphs)."""
         self._host_graph_replay(self._step_host_eager, q_host, out_host, q_dev, stream)
 
 

@@ -149,6 +149,18 @@ int entmaxkv_select(const float* page_scores, const ekv_paged_kv* kv, int32_t nu
 }
 
 // Checks of a decode call's arguments; on success *L is its workspace layout.
+// The device can read and write p: device or managed memory, or host memory
+// mapped into the device's address space (pinned, unified addressing).
+static bool device_accessible(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
 static int check_decode(const float* q, int32_t num_q_heads, float scale, const ekv_paged_kv* kv,
                         const int32_t* sel, const int32_t* n_sel, int32_t cap_pages, float alpha,
                         const float* out, const void* workspace, size_t ws_bytes,
@@ -165,6 +177,7 @@ static int check_decode(const float* q, int32_t num_q_heads, float scale, const 
     *L = ekv::decode_layout(kv->batch, num_q_heads, kv->num_kv_heads, kv->head_dim,
                             kv->page_size, kv->max_pages, cap_pages);
     if (ws_bytes < L->total) return EKV_WORKSPACE_TOO_SMALL;
+    if (!device_accessible(out)) return EKV_INVALID_ARG;   // last: one host query
     return EKV_OK;
 }
 
@@ -342,6 +355,13 @@ int entmaxkv_read_device_status(int32_t* status_out, void* stream) {
     if (e != cudaSuccess) return EKV_CUDA_ERROR;
     *status_out = (flag & 2) ? EKV_DEVICE_TIMEOUT : (flag & 1) ? EKV_DEVICE_CHECK_FAILED : EKV_OK;
     return EKV_OK;
+}
+
+int entmaxkv_copy_in(void* dst, const void* src, size_t bytes, void* stream) {
+    if (!dst || !src) return EKV_INVALID_ARG;
+    if (bytes == 0) return EKV_OK;
+    if (!device_accessible(dst) || !device_accessible(src)) return EKV_INVALID_ARG;
+    return from_cuda(ekv::launch_copy_in(dst, src, bytes, static_cast<cudaStream_t>(stream)));
 }
 
 int entmaxkv_check_wait_timeout(uint32_t limit_us, void* stream) {

@@ -116,6 +116,10 @@ cudaError_t take_status_selfcheck(int* flag, cudaStream_t s);
 // after limit_ns and records the timeout bit (self-check of the give-up path).
 cudaError_t launch_wait_timeout_check(uint64_t limit_ns, cudaStream_t s);
 
+// Copies `bytes` from src to dst (both device-accessible) with a kernel that
+// lets the next kernel of the stream start early (programmatic launch).
+cudaError_t launch_copy_in(void* dst, const void* src, size_t bytes, cudaStream_t s);
+
 // Limits of the selection kernels (pages held in shared memory per head).
 constexpr int kMaxPagesTopk = 49152;
 constexpr int kMaxPagesGauss = 12288;

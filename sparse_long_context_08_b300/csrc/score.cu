@@ -192,6 +192,7 @@ score_kernel(const float* __restrict__ q, int Hq, float scale, KV kv,
             const bool live = inr && sblk[j] >= 0;
             const int b = ref >> 17;
             if (inr && b != cur_b) {
+                pdl_wait();                    // q may be the previous kernel's output
                 cur_b = b;
                 const float* qh = q + ((int64_t)b * Hq + kvh * G) * D + lt * C::DPL;
 #pragma unroll
@@ -516,6 +517,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
                     if (lane == 0) flag_timeout();
                     break;
                 }
+                pdl_wait();                            // q may be the previous kernel's output
                 tc_build_b<D, G, HKV, kTcProd>(bbuf, q, scale, b_cur, tid);
                 bseq = b_cur;
                 fence_proxy_async_smem();              // B, written by this thread
@@ -572,6 +574,7 @@ score_bbox_tc_kernel(const bf16raw* __restrict__ kmin, const bf16raw* __restrict
         if (nt > 0) {                                  // B of the first tile's sequence
             int b, p0, npg;
             tc_tile<PPT>(t0, tps, kv, b, p0, npg);
+            pdl_wait();                                // q may be the previous kernel's output
             tc_build_b<D, G, HKV, 128>(bbuf, q, scale, b, tid - (kTcMmaWarp + 1) * 32);
             fence_proxy_async_smem();
             mbar_arrive(&sh.binit);
@@ -637,7 +640,7 @@ static cudaError_t launch_score_tc_t(const float* q, float scale, const KV& kv, 
     cudaError_t e = cudaFuncSetAttribute(score_bbox_tc_kernel<D, G, HKV>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(score_bbox_tc_kernel<D, G, HKV>, dim3(sm_count_score()), dim3(kTcThreads),
+    return launch_kernel_pdl(score_bbox_tc_kernel<D, G, HKV>, dim3(sm_count_score()), dim3(kTcThreads),
                          smem, s, static_cast<const bf16raw*>(kmin),
                          static_cast<const bf16raw*>(kmax), q, scale, kv, out);
 }
@@ -667,7 +670,7 @@ static cudaError_t launch_score_t(const float* q, int Hq, float scale, const KV&
     cudaError_t e = cudaFuncSetAttribute(score_kernel<T, D, G, kGauss>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(score_kernel<T, D, G, kGauss>, dim3(grid), dim3(kScoreThreads), smem, s, q, Hq,
+    return launch_kernel_pdl(score_kernel<T, D, G, kGauss>, dim3(grid), dim3(kScoreThreads), smem, s, q, Hq,
                          scale, kv, static_cast<const T*>(ma), static_cast<const T*>(mb), out,
                          nloc_max);
 }

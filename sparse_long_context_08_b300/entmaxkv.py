@@ -35,7 +35,8 @@ SYMBOLS = ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select"
            "entmaxkv_decode_counts", "entmaxkv_decode_noalloc", "entmaxkv_decode_full",
            "entmaxkv_full_workspace_size", "entmaxkv_decode_softmax",
            "entmaxkv_decode_softmax_full", "entmaxkv_softmax_workspace_size",
-           "entmaxkv_kept_mass", "entmaxkv_check_wait_timeout", "entmaxkv_select_decode")
+           "entmaxkv_kept_mass", "entmaxkv_check_wait_timeout", "entmaxkv_select_decode",
+           "entmaxkv_copy_in")
 
 
 class EntmaxKVError(RuntimeError):
@@ -92,12 +93,13 @@ def lib() -> C.CDLL:
         L.entmaxkv_check_wait_timeout.argtypes = [C.c_uint32, vp]
         L.entmaxkv_select_decode.argtypes = [vp, vp, i32, f32, vp, i32, i32, f32, f32, vp, vp,
                                              vp, vp, vp, vp, vp, sz, vp]
+        L.entmaxkv_copy_in.argtypes = [vp, vp, sz, vp]
         for name in ("entmaxkv_build_page_meta", "entmaxkv_score_pages", "entmaxkv_select",
                      "entmaxkv_decode", "entmaxkv_read_device_status",
                      "entmaxkv_set_stage_events", "entmaxkv_decode_counts", "entmaxkv_decode_noalloc",
                      "entmaxkv_decode_full", "entmaxkv_decode_softmax",
                      "entmaxkv_decode_softmax_full", "entmaxkv_kept_mass",
-                     "entmaxkv_check_wait_timeout", "entmaxkv_select_decode"):
+                     "entmaxkv_check_wait_timeout", "entmaxkv_select_decode", "entmaxkv_copy_in"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -111,14 +113,16 @@ def _ptr(t: torch.Tensor | None):
     return None if t is None else C.c_void_p(t.data_ptr())
 
 
-def _need(t: torch.Tensor, name: str, dtype: torch.dtype | tuple, shape: tuple | None = None):
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype | tuple, shape: tuple | None = None,
+          pinned_ok: bool = False):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     dts = dtype if isinstance(dtype, tuple) else (dtype,)
     if t.dtype not in dts:
         raise TypeError(f"{name}: dtype {t.dtype}, expected {dts}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_cuda and not (pinned_ok and t.is_pinned()):
+        raise ValueError(f"{name} must be on a CUDA device" + (" or in pinned host memory"
+                                                               if pinned_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
@@ -314,7 +318,7 @@ def entmaxkv_select_decode(page_scores: torch.Tensor, q: torch.Tensor, num_q_hea
     _need(n_sel, "n_sel", torch.int32, (kv.batch, num_q_heads))
     if aux is not None:
         _need(aux, "aux", torch.float32, (kv.batch, num_q_heads, 2))
-    _need(out, "out", torch.float32, (kv.batch, num_q_heads, kv.head_dim))
+    _need(out, "out", torch.float32, (kv.batch, num_q_heads, kv.head_dim), pinned_ok=True)
     if tau_out is not None:
         _need(tau_out, "tau_out", torch.float32, (kv.batch, num_q_heads))
     if support_out is not None:
@@ -400,6 +404,19 @@ def entmaxkv_read_device_status(stream=None) -> int:
     _check("entmaxkv_read_device_status",
            lib().entmaxkv_read_device_status(C.byref(st), _stream(stream)))
     return int(st.value)
+
+
+def entmaxkv_copy_in(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    """Copy src (device memory or pinned host memory) into dst (same size)
+    with a kernel instead of a copy engine: a step captured after it has no
+    copy-engine hand-off, and the score kernel sets up while it runs."""
+    if src.numel() * src.element_size() != dst.numel() * dst.element_size():
+        raise ValueError("entmaxkv_copy_in: src and dst differ in size")
+    if not src.is_contiguous() or not dst.is_contiguous():
+        raise ValueError("entmaxkv_copy_in: src and dst must be contiguous")
+    _check("entmaxkv_copy_in", lib().entmaxkv_copy_in(_ptr(dst), _ptr(src),
+                                                      dst.numel() * dst.element_size(),
+                                                      _stream(stream)))
 
 
 def entmaxkv_check_wait_timeout(limit_us: int, stream=None) -> None:

@@ -532,3 +532,35 @@ def test_graph_capture_replays_the_step():
     out = g.dec.out.cpu().numpy().astype(np.float64).reshape(ref["out"].shape)
     assert np.array_equal(out, ref["out"])
 
+
+
+def test_copy_in_from_pinned_host_memory():
+    """The input-staging kernel copies pinned host memory (16-byte path and
+    byte path, misaligned views included) exactly; pageable host memory is
+    rejected on the host, before any launch."""
+    gen = torch.Generator().manual_seed(5)
+    for n in (1, 15, 16, 1000, 4099, 1 << 17):
+        src = torch.randint(0, 256, (n + 1,), dtype=torch.uint8, generator=gen).pin_memory()
+        for view in (src[:n], src[1:]):
+            dst = torch.zeros(n, dtype=torch.uint8, device="cuda")
+            E.entmaxkv_copy_in(dst, view)
+            torch.cuda.synchronize()
+            assert torch.equal(dst.cpu(), view), n
+    pageable = torch.zeros(64, dtype=torch.uint8)
+    with pytest.raises(E.EntmaxKVError):
+        E.entmaxkv_copy_in(torch.zeros(64, dtype=torch.uint8, device="cuda"), pageable)
+
+
+def test_select_decode_writes_pinned_host_output():
+    """out in pinned host memory is written by the decode kernel directly and
+    equals the device-memory result bit for bit."""
+    w = make_workload("long128k", batch=2, context=8192)
+    g = GpuRun(w)
+    g.dec.score(g.q)
+    g.dec.select_decode(g.q)
+    torch.cuda.synchronize()
+    ref = g.dec.out.cpu().clone()
+    host = torch.full(g.dec.out.shape, float("nan"), dtype=torch.float32).pin_memory()
+    g.dec.select_decode(g.q, out=host)
+    torch.cuda.synchronize()
+    assert torch.equal(host, ref)

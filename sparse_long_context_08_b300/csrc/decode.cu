@@ -634,11 +634,12 @@ constexpr int kTpvPruneTokens = 2048;  // candidate pages' tokens above which t 
 
 // Union pages i < ucnt of a head whose largest z' exceeds max - 1 (only those
 // can hold a token with nonzero weight), written to list[] in a fixed thread
-// order; returns their count.  pm[] holds the first round of maxima (entries
+// order (and, with list_x, their maxima minus max); returns their count.  pm[] holds the first round of maxima (entries
 // j * blockDim + tid); later rounds are read from pmr (page i at pmr[i]).
 // Every thread calls it.
 __device__ int list_candidate_pages(float (&pm)[kTpvPmVec], const float* __restrict__ pmr,
-                                    int ucnt, float mx, int* list, int* ired) {
+                                    int ucnt, float mx, int* list, int* ired,
+                                    float* list_x = nullptr) {
     const int tid = threadIdx.x, nt = blockDim.x;
     int npl = 0;
     for (int p0 = 0; p0 < ucnt; p0 += kTpvPmVec * nt) {
@@ -657,7 +658,10 @@ __device__ int list_candidate_pages(float (&pm)[kTpvPmVec], const float* __restr
 #pragma unroll
         for (int j = 0; j < kTpvPmVec; ++j) {
             const int i = p0 + j * nt + tid;
-            if (i < ucnt && pm[j] - mx > -1.f) list[pos++] = i;
+            if (i < ucnt && pm[j] - mx > -1.f) {
+                if (list_x) list_x[pos] = pm[j] - mx;
+                list[pos++] = i;
+            }
         }
         npl += tot;
     }
@@ -976,7 +980,9 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
         }
         return;
     }
-    int npl = list_candidate_pages(pm, pmr, ucnt, mx, s_pl, ired);   // ends with a barrier
+    // the pages' maxima go to s_x as well when it can hold every union page
+    int npl = list_candidate_pages(pm, pmr, ucnt, mx, s_pl, ired,
+                                   L.Umax <= cand_cap ? s_x : nullptr);   // ends with a barrier
 
     // 1b. many candidate tokens: a lower bound of t from the candidate pages'
     // maxima (scores of tokens of the head): their own threshold t_S solves
@@ -984,9 +990,7 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
     // t_S hold no token of the support and are dropped, tokens at or below it
     // are not candidates, and the solve below starts from t_S.
     float tlo = -1.f;
-    if (E != 0 && (npl << pshift) > kTpvPruneTokens && npl <= cand_cap) {
-        for (int k = tid; k < npl; k += kTpvThreads) s_x[k] = __ldcg(pmr + s_pl[k]) - mx;
-        __syncthreads();
+    if (E != 0 && (npl << pshift) > kTpvPruneTokens && L.Umax <= cand_cap) {
         float ts;
         if (npl <= 1024) {
             if (wid == 0) {

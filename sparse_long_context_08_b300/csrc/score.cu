@@ -29,7 +29,7 @@ namespace ekv {
 
 constexpr int kScoreWarps = 8;
 constexpr int kScoreThreads = 32 * kScoreWarps;
-constexpr int kScoreCtasPerSm = 2;
+constexpr int kScoreCtasPerSm = 2;   // fp32 rows with G <= 4 take ScoreCfg::CTAS = 3
 constexpr int kScoreStages = 8;                             // row pairs in flight per lane
 constexpr int kScoreMaxSeqs = 16384;
 
@@ -65,6 +65,9 @@ struct ScoreCfg {
     static constexpr int LPR = D / DPL;                         // lanes per row
     static constexpr int PPP = 32 / LPR;                        // pages per warp pass
     static constexpr int NV = kGauss ? 2 * G : G;               // sums per row
+    // CTAs per SM: a third for fp32 rows of up to 4 heads per kv head (they fit
+    // 80 registers; more warps hide the per-row chain of shuffles)
+    static constexpr int CTAS = (ES == 4 && G <= 4) ? 3 : kScoreCtasPerSm;
     static_assert(LPR <= 32 && NV <= LPR, "unsupported score shape");
 };
 
@@ -102,7 +105,7 @@ __device__ __forceinline__ void widen_lane(const void* p, float* x) {
 }
 
 template <typename T, int D, int G, bool kGauss>
-__global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm)
+__global__ void __launch_bounds__(kScoreThreads, (ScoreCfg<T, D, G, kGauss>::CTAS))
 score_kernel(const float* __restrict__ q, int Hq, float scale, KV kv,
              const T* __restrict__ ma,      // bbox: kmin   gauss: mean
              const T* __restrict__ mb,      // bbox: kmax   gauss: var
@@ -660,10 +663,10 @@ template <typename T, int D, int G, bool kGauss>
 static cudaError_t launch_score_t(const float* q, int Hq, float scale, const KV& kv,
                                   const void* ma, const void* mb, float* out, cudaStream_t s) {
     if (kv.B > kScoreMaxSeqs || kv.maxp >= (1 << 17)) return kShapeUnsupported;
-    const int grid = sm_count_score() * kScoreCtasPerSm;
+    using C = ScoreCfg<T, D, G, kGauss>;
+    const int grid = sm_count_score() * C::CTAS;
     const int64_t total_max = (int64_t)kv.B * kv.maxp;
     const int nloc_max = (int)((total_max + grid - 1) / grid) + 1;
-    using C = ScoreCfg<T, D, G, kGauss>;
     const size_t ring_bytes = (size_t)kScoreWarps * kScoreStages * 2 * 32 * C::DPL * sizeof(T);
     const size_t smem = ring_bytes + (size_t)(kv.B + 1 + 2 * nloc_max) * sizeof(int);
     if (smem > 110 * 1024) return kShapeUnsupported;

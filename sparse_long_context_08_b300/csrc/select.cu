@@ -851,8 +851,18 @@ select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float 
     const float* src = ms + (int64_t)bh * kv.maxp * 2;
     pdl_wait();                         // the page scores are the previous kernel's output
     float mu_max = -INFINITY;
-    for (int p = threadIdx.x; p < np; p += blockDim.x) {
-        const float m = src[2 * p], s = src[2 * p + 1];
+    // every page's (m, s) in flight at once (KPT pages per thread, strided)
+    float2 msv[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int p = j * kSelThreads + threadIdx.x;
+        msv[j] = p < np ? __ldcg(reinterpret_cast<const float2*>(src) + p) : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int p = j * kSelThreads + threadIdx.x;
+        if (p >= np) continue;
+        const float m = msv[j].x, s = msv[j].y;
         const int n = min(kv.P, len - p * kv.P);
         const float zmax = n > 1 ? fmaf(sqrtf(2.f * logf(static_cast<float>(n))), s, m) : m;
         s_mu[p] = c * m;

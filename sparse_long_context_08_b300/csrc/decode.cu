@@ -45,7 +45,7 @@ constexpr int kTpvgThreads = 512;                      // the global-candidate v
 constexpr int kTpvVec = 8;                             // float4 per thread per score tile
 constexpr int kTpvTile = kTpvThreads * kTpvVec * 4;    // scores per tile
 constexpr int kTpvgTile = kTpvgThreads * kTpvVec * 4;
-constexpr int kTpvgRows = 4;                           // V rows in flight per row group (tpv kernels)
+constexpr int kTpvgRows = 8;                           // V rows in flight per row group (tpv kernels)
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

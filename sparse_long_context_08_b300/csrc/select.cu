@@ -858,16 +858,18 @@ select_gauss_kernel(const float* __restrict__ ms, KV kv, int Hq, int cap, float 
         const int p = j * kSelThreads + threadIdx.x;
         msv[j] = p < np ? __ldcg(reinterpret_cast<const float2*>(src) + p) : make_float2(0.f, 0.f);
     }
+    const float zfull = sqrtf(2.f * logf(static_cast<float>(kv.P)));   // a full page's factor
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
         const int p = j * kSelThreads + threadIdx.x;
         if (p >= np) continue;
         const float m = msv[j].x, s = msv[j].y;
         const int n = min(kv.P, len - p * kv.P);
-        const float zmax = n > 1 ? fmaf(sqrtf(2.f * logf(static_cast<float>(n))), s, m) : m;
+        const float zf = n == kv.P ? zfull : (n > 1 ? sqrtf(2.f * logf(static_cast<float>(n))) : 0.f);
+        const float zmax = n > 1 ? fmaf(zf, s, m) : m;
         s_mu[p] = c * m;
         s_sg[p] = c * s;
-        s_isg[p] = c * s > 0.f ? 1.f / (c * s) : 0.f;
+        s_isg[p] = c * s > 0.f ? __frcp_rn(c * s) : 0.f;
         keys[p] = float_key(zmax);
         mu_max = fmaxf(mu_max, c * m);
     }

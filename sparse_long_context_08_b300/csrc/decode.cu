@@ -630,7 +630,7 @@ qk_mma_kernel(const float* __restrict__ q, int Hq, float qscale, KV kv, WS ws, D
 // tpv: exact alpha-entmax threshold and value accumulation, one CTA per head
 // ---------------------------------------------------------------------------
 constexpr int kTpvPmVec = 8;          // page maxima per thread per round trip
-constexpr int kTpvPruneTokens = 2048;  // candidate pages' tokens above which t is first bounded
+constexpr int kTpvPruneTokens = 4096;  // candidate pages' tokens above which t is first bounded
 
 // Union pages i < ucnt of a head whose largest z' exceeds max - 1 (only those
 // can hold a token with nonzero weight), written to list[] in a fixed thread
@@ -956,21 +956,19 @@ tpv_kernel(int Hq, float alpha, int cand_cap, KV kv, WS ws, DecodeLayout L,
     if (tid == 0) prefetch_l2_line(ws.union_count + u);
     pdl_wait();                               // the scores are the previous kernel's output
     const int ucnt = __ldcg(ws.union_count + u);
+    // the head's largest z', which q.K accumulated from the same scores as the
+    // page maxima (0: the head has no selected token)
+    const uint32_t hkey = __ldcg(ws.head_max + bh);
     float pm[kTpvPmVec];
 #pragma unroll
     for (int j = 0; j < kTpvPmVec; ++j) {
         const int i = j * kTpvThreads + tid;
         pm[j] = i < L.Umax ? __ldcg(pmr + i) : -INFINITY;
     }
-    float mxl = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kTpvPmVec; ++j) {
-        if (j * kTpvThreads + tid < ucnt) mxl = fmaxf(mxl, pm[j]);
-        else pm[j] = -INFINITY;
-    }
-    for (int i = kTpvPmVec * kTpvThreads + tid; i < ucnt; i += kTpvThreads)
-        mxl = fmaxf(mxl, __ldcg(pmr + i));
-    const float mx = block_max(mxl, fred);
+    for (int j = 0; j < kTpvPmVec; ++j)
+        if (j * kTpvThreads + tid >= ucnt) pm[j] = -INFINITY;
+    const float mx = hkey ? key_float(hkey) : -INFINITY;
     if (!(mx > -INFINITY)) {                  // no selected token
         for (int i = tid; i < D; i += blockDim.x) outb[i] = 0.f;
         if (tid == 0) {

@@ -699,15 +699,14 @@ __device__ __forceinline__ bool threshold_step(float f, float d, float h, float&
 }
 
 // The threshold t of the m candidates x (relative to the max; e = 1, 2) by
-// threshold_step, every thread of the block taking part.
-// The same by one warp for m <= 1024 candidates (32 per lane in registers,
-// shuffle-only reductions), from the bracket [t0, 0] (f(t0) >= 0).
-template <int E>
-__device__ float warp_threshold(const float* s_vals, int m, float t0) {
+// threshold_step, by one warp for m <= 32 * NR candidates (NR per lane in
+// registers, shuffle-only reductions), from the bracket [t0, 0] (f(t0) >= 0).
+template <int E, int NR>
+__device__ float warp_threshold_n(const float* s_vals, int m, float t0) {
     const int lane = threadIdx.x & 31;
-    float xr[32];
+    float xr[NR];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < NR; ++j) {
         const int i = j * 32 + lane;
         xr[j] = i < m ? s_vals[i] : -INFINITY;
     }
@@ -715,7 +714,7 @@ __device__ float warp_threshold(const float* s_vals, int m, float t0) {
     for (int it = 0; it < 64; ++it) {
         float s0 = 0.f, s1 = 0.f, s2 = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < NR; ++j) {
             const float a = xr[j] - tt;
             if (a > 0.f) {
                 if (E == 2) { s0 = fmaf(a, a, s0); s1 += a; s2 += 1.f; }
@@ -730,7 +729,15 @@ __device__ float warp_threshold(const float* s_vals, int m, float t0) {
     }
     return tt;
 }
+// m <= 1024: as few registers per lane as the candidates need
+template <int E>
+__device__ float warp_threshold(const float* s_vals, int m, float t0) {
+    if (m <= 64) return warp_threshold_n<E, 2>(s_vals, m, t0);
+    if (m <= 256) return warp_threshold_n<E, 8>(s_vals, m, t0);
+    return warp_threshold_n<E, 32>(s_vals, m, t0);
+}
 
+// The same with every thread of the block taking part (any m).
 template <int E, bool kGlobal>
 __device__ float solve_threshold(const float* x, int m, float4* red, float t0 = -1.f) {
     float t = t0, lo = t0, hi = 0.f;

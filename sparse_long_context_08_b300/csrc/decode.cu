@@ -42,7 +42,7 @@ constexpr int kQkSmemBudget = 220 * 1024;
 constexpr int kMaxUnits = 8192;                        // qk keeps a prefix over units in smem
 constexpr int kTpvThreads = 256;
 constexpr int kTpvgThreads = 512;                      // the global-candidate variant
-constexpr int kTpvVec = 8;                             // float4 per thread per score tile
+constexpr int kTpvVec = 2;                             // float4 per thread per score tile (short: tpv's code runs cold)
 constexpr int kTpvTile = kTpvThreads * kTpvVec * 4;    // scores per tile
 constexpr int kTpvgTile = kTpvgThreads * kTpvVec * 4;
 constexpr int kTpvgRows = 8;                           // V rows in flight per row group (tpv kernels)

@@ -35,7 +35,7 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy()
 
 
-class GpuRun:
+class DeviceRun:
     """The CUDA pipeline on one workload, plus numpy copies of every stage."""
 
     def __init__(self, w, device="cuda"):

@@ -11,7 +11,7 @@ import oracle
 from sparse_long_context_08_b300 import entmaxkv as E
 from sparse_long_context_08_b300.workloads import make_workload
 
-from gpu_util import (GpuRun, bbox_scale, compare_decode, compare_meta, compare_scores,
+from gpu_util import (DeviceRun, bbox_scale, compare_decode, compare_meta, compare_scores,
                       compare_selection, compare_support, gauss_scale, record_ties)
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +27,7 @@ def _cuda():
 
 def full_parity(w, heads=None, check_e2e=True):
     """Every stage of one decode step against the oracle; returns report dict."""
-    g = GpuRun(w)
+    g = DeviceRun(w)
     r = g.step()
     kv = oracle.KV(w)
     om = oracle.build_meta(kv)
@@ -341,7 +341,7 @@ def test_budget_covers_every_page_and_single_page_sequences():
     w = make_workload("long128k", batch=3, seq_lens=[5 * 32, 20, 1], budget_tokens=4096,
                       planted_pages=0)
     rep = full_parity(w)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     r = g.step()
     for bh in range(w.batch * w.num_q_heads):
         np_ = w.pages_of(bh // w.num_q_heads)
@@ -354,7 +354,7 @@ def test_zero_length_sequence_in_a_batch():
     +inf, support 0, on every path; the other sequences match the oracle."""
     w = make_workload("long128k", batch=3, seq_lens=[5000, 0, 3000], planted_pages=2)
     rep = full_parity(w, heads=[h for h in range(3 * w.num_q_heads) if h // w.num_q_heads != 1])
-    g = GpuRun(w)
+    g = DeviceRun(w)
     r = g.step()
     Hq = w.num_q_heads
     assert np.all(r["n_sel"][Hq:2 * Hq] == 0)
@@ -373,7 +373,7 @@ def test_zero_length_sequence_in_a_batch():
 
 def test_empty_selection_gives_zero_output():
     w = make_workload("long128k", batch=1, context=2048)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     g.step()
     BH = w.num_q_heads
     sel = np.zeros((BH, w.cap_pages), np.int32)
@@ -392,7 +392,7 @@ def test_tie_storm_constant_keys():
     gets the same weight, so out is the mean of the kept values."""
     w = make_workload("long128k", batch=1, context=32 * 40, planted_pages=0, budget_tokens=32 * 7)
     w.k_pool[:] = w.k_pool[0, 0, 0]
-    g = GpuRun(w)
+    g = DeviceRun(w)
     r = g.step()
     kv = oracle.KV(w)
     for bh in range(w.num_q_heads):
@@ -412,7 +412,7 @@ def test_sparsemax_single_token_support():
     for h in range(8):
         qn = w.q[0, h] / np.linalg.norm(w.q[0, h])
         w.k_pool[blk, h, 5] = 40.0 * qn
-    g = GpuRun(w)
+    g = DeviceRun(w)
     r = g.step()
     assert np.all(r["support"] == 1)
     for h in range(8):
@@ -423,7 +423,7 @@ def test_sparsemax_single_token_support():
 def test_bad_page_table_entry_is_flagged_not_faulted():
     w = make_workload("long128k", batch=1, context=2048, planted_pages=0)
     w.page_table[0, 10] = w.num_blocks + 5     # out of range
-    g = GpuRun(w)
+    g = DeviceRun(w)
     g.step()
     assert E.entmaxkv_read_device_status() == E.EKV_DEVICE_CHECK_FAILED
     assert E.entmaxkv_read_device_status() == E.EKV_OK     # read clears it
@@ -445,7 +445,7 @@ def test_select_decode_matches_the_separate_calls(name, over):
     Gaussian selection and long contexts keep the decode's own plan) returns,
     bit for bit, what entmaxkv_select followed by entmaxkv_decode returns."""
     w = make_workload(name, **over)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     d = g.dec
     d.score(g.q)
     d.select()
@@ -486,7 +486,7 @@ def test_bounded_wait_timeout_is_reported_and_the_context_survives():
 
 def test_deterministic_across_runs():
     w = make_workload("long128k", batch=2, context=8192)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     a = g.step()
     b = g.step()
     for k in ("page_scores", "sel", "n_sel", "out", "tau", "support"):
@@ -498,7 +498,7 @@ def test_step_host_graph_matches_the_device_step():
     graph; every call returns what the device step returns, bit for bit, and
     follows new host inputs."""
     w = make_workload("long128k", batch=2, context=8192)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     q_host = g.q.cpu().pin_memory()
     out_host = torch.empty(g.dec.out.shape, dtype=torch.float32).pin_memory()
     q_dev = torch.empty_like(g.q)
@@ -515,7 +515,7 @@ def test_step_host_graph_matches_the_device_step():
 
 def test_graph_capture_replays_the_step():
     w = make_workload("long128k", batch=2, context=8192)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     ref = g.step()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -555,7 +555,7 @@ def test_select_decode_writes_pinned_host_output():
     """out in pinned host memory is written by the decode kernel directly and
     equals the device-memory result bit for bit."""
     w = make_workload("long128k", batch=2, context=8192)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     g.dec.score(g.q)
     g.dec.select_decode(g.q)
     torch.cuda.synchronize()
